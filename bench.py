@@ -1,0 +1,451 @@
+#!/usr/bin/env python3
+"""Benchmark of the NVFP4 sparse-MLA decode hot path on GB300.
+
+One step = one pass of the whole path over one batch: quantize-and-append the batch's new
+KV tokens (one per query row) into the paged NVFP4 pool, then sparse MLA decode of every
+query row (gather, dequant, QK^T, online softmax, PV, split merge).
+
+Workload (N=1 line): B=32 decode rows, s_q=1, h_q=128, topk=2048, 352-B records, a paged pool
+of 2,097,152 slots (32,768 pages of 64 tokens, 738 MB), each sequence 65,536 tokens long.
+Eight independent index/query sets rotate between steps, so one lap gathers ~185 MB of
+distinct records -- more than the 126 MB L2 -- and every step reads its records from HBM.
+
+Prints one JSON line (rank 0). Multi-GPU (torchrun, N ranks): each rank runs its own replica
+on its own batch (query rows shard with no exchange), value = rows of all ranks / max time.
+`--impl reference` times the CPU oracle on a bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "NVFP4 sparse-MLA decode query-tokens/s and % roofline (h_q128,topk2048, 1×GB300)"
+UNIT = "query-tokens/s"
+N_SETS = 8
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+# DRAM traffic of one decode call (both kernels) from an ncu capture of this workload, keyed
+# by the hash of the decode source it was taken with; reported as null once the source moves.
+NCU_TRAFFIC = {}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return PEAKS_FALLBACK, "fallback"
+
+
+def decode_source_hash() -> str:
+    src = os.path.join(ROOT, "nvfp4_kv_cache_sparse_gb300", "csrc", "sparse_decode.cu")
+    return hashlib.sha1(open(src, "rb").read()).hexdigest()[:12]
+
+
+# ---------------------------------------------------------------------------------------
+# distributed plumbing
+# ---------------------------------------------------------------------------------------
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world: int, backend: str):
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend)
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(value: float, world: int, device) -> float:
+    """Max of a per-rank scalar over all ranks (the slowest rank sets the job time)."""
+    if world == 1:
+        return value
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(rows_per_rank: int, world: int, max_seconds: float) -> float:
+    """Weak scaling: every rank processes its own rows; the job takes the slowest rank's time."""
+    return rows_per_rank * world / max_seconds
+
+
+# ---------------------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for name, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------------------
+# workload
+# ---------------------------------------------------------------------------------------
+
+def roofline_numbers(w: synth.DecodeWorkload):
+    rows = w.n_rows
+    flops = 2.0 * w.h_q * w.topk * (576 + 512) * rows
+    bytes_ = rows * (w.topk * w.record_bytes + w.h_q * 576 * 2 + w.topk * 4)
+    return flops, bytes_
+
+
+def make_sets(seed: int):
+    """N_SETS decode batches over one pool (same pages, different queries and index lists)."""
+    sets = [synth.batch_decode(seed=seed + k) for k in range(N_SETS)]
+    # one pool for all sets: pool_seed and geometry come from the first set
+    base = sets[0]
+    for s in sets:
+        s.pool_seed = base.pool_seed
+    return sets
+
+
+def new_token_batch(w: synth.DecodeWorkload, step_seed: int):
+    rng = np.random.default_rng(10_000 + step_seed)
+    lat = synth.bf16_from_f32(rng.standard_normal((w.n_rows, 512), dtype=np.float32))
+    rope = synth.bf16_from_f32(rng.standard_normal((w.n_rows, 64), dtype=np.float32))
+    slots = torch.from_numpy(rng.choice(w.num_slots, size=w.n_rows, replace=False).astype(np.int64))
+    return lat, rope, slots
+
+
+# ---------------------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------------------
+
+def run_gpu(args):
+    import nvfp4_kv_cache_sparse_gb300 as lib
+    from synth.pool import fill_pool
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    init_dist(world, "nccl")
+    lib.load()
+
+    sets = make_sets(seed=rank * 100)
+    w0 = sets[0]
+    cache = fill_pool(lib.quantize_append, w0.num_slots, w0.record_bytes, w0.pool_seed, dev)
+    qs = [s.q.to(dev) for s in sets]
+    idxs = [s.indices.to(dev) for s in sets]
+    news = [tuple(t.to(dev) for t in new_token_batch(w0, k)) for k in range(N_SETS)]
+    splits = 0
+    ws_bytes = lib.workspace_size(w0.B, w0.s_q, w0.h_q, w0.topk, w0.record_bytes, splits)
+    workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+    out = torch.empty((w0.B, w0.s_q, w0.h_q, 512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((w0.B, w0.s_q, w0.h_q), dtype=torch.float32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+    launches_per_step = 2 + (1 if ws_bytes > 0 else 0)
+
+    def step(k, ev=None):
+        lat, rope, slots = news[k % N_SETS]
+        lib.quantize_append(lat, rope, slots, cache, dev_status=status, stream=stream)
+        if ev is not None:
+            ev[0].record(stream)
+        lib.sparse_mla_decode(qs[k % N_SETS], cache, idxs[k % N_SETS], w0.sm_scale, out=out, lse=lse,
+                              num_splits=splits, workspace=workspace, dev_status=status, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+
+    for k in range(args.warmup):
+        step(k)
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} after warm-up")
+
+    # ---- device-timed steps (inputs resident in HBM)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(torch.cuda.current_device() if world == 1 else local)
+    barrier(world)
+    torch.cuda.synchronize()
+    with sampler:
+        start.record(stream)
+        for k in range(args.steps):
+            step(args.warmup + k, evs[k])
+        end.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+    t_local = start.elapsed_time(end) / 1e3
+    t_job = max_over_ranks(t_local, world, dev)
+    decode_ms = [a.elapsed_time(b) for a, b in evs]
+    decode_s = statistics.mean(decode_ms) / 1e3
+    clocks = sampler.summary()
+
+    # ---- end to end through the public API with host buffers
+    pin = lambda t: t.pin_memory()
+    host_q = [pin(s.q) for s in sets]
+    host_idx = [pin(s.indices) for s in sets]
+    host_new = [tuple(pin(t) for t in new_token_batch(w0, k)) for k in range(N_SETS)]
+    host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    host_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    d_q = torch.empty_like(qs[0])
+    d_idx = torch.empty_like(idxs[0])
+    d_new = [torch.empty_like(t) for t in news[0]]
+
+    def e2e_step(k):
+        j = k % N_SETS
+        d_q.copy_(host_q[j], non_blocking=True)
+        d_idx.copy_(host_idx[j], non_blocking=True)
+        for d, h in zip(d_new, host_new[j]):
+            d.copy_(h, non_blocking=True)
+        lib.quantize_append(d_new[0], d_new[1], d_new[2], cache, stream=stream)
+        lib.sparse_mla_decode(d_q, cache, d_idx, w0.sm_scale, out=out, lse=lse, num_splits=splits,
+                              workspace=workspace, stream=stream)
+        host_out.copy_(out, non_blocking=True)
+        host_lse.copy_(lse, non_blocking=True)
+
+    for k in range(args.warmup):
+        e2e_step(k)
+    torch.cuda.synchronize()
+    barrier(world)
+    s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s2.record(stream)
+    for k in range(args.steps):
+        e2e_step(k)
+    e2.record(stream)
+    torch.cuda.synchronize()
+    t_e2e = max_over_ranks(s2.elapsed_time(e2) / 1e3, world, dev)
+    h2d = sum(t.numel() * t.element_size() for t in (host_q[0], host_idx[0]) + host_new[0])
+    d2h = host_out.numel() * host_out.element_size() + host_lse.numel() * host_lse.element_size()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} after timing")
+
+    result = None
+    if rank == 0:
+        peaks, peak_src = load_peaks()
+        flops, alg_bytes = roofline_numbers(w0)
+        achieved = flops / decode_s / 1e12
+        peak = float(peaks["bf16_tflops"])
+        traffic = NCU_TRAFFIC.get(decode_source_hash())
+        cpu = cpu_baseline(args, w0) if (world == 1 and not args.no_cpu_baseline) else None
+        result = {
+            "metric": METRIC,
+            "value": job_throughput(w0.n_rows * args.steps, world, t_job),
+            "unit": UNIT,
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": t_job / args.steps * 1e3,
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "bf16",
+            "data": "synthetic",
+            "config": {
+                "workload": w0.name,
+                "batch": w0.B, "s_q": w0.s_q, "h_q": w0.h_q, "topk": w0.topk, "record_bytes": w0.record_bytes,
+                "pool_slots": w0.num_slots, "page_tokens": synth.PAGE, "seq_len": int(w0.seq_lens[0]),
+                "appended_tokens_per_step": w0.n_rows, "num_splits": "auto",
+                "l2": f"inputs larger than L2: {N_SETS} rotating index/query sets gather "
+                      f"{N_SETS * w0.n_rows * w0.topk * w0.record_bytes / 1e6:.0f} MB of records per lap",
+                "parallelism": f"replicas x{world}",
+            },
+            "roofline": {
+                "bound": "tensor",
+                "achieved": achieved,
+                "peak": peak,
+                "unit": "TFLOP/s",
+                "frac": achieved / peak,
+                "traffic": traffic,
+                "kernel": "decode call (sparse_decode_kernel + combine_kernel), CUDA events on the launch stream",
+                "peak_source": f"{peak_src} bf16 burst",
+                "decode_us": decode_s * 1e6,
+                "roofline_us": max(flops / (peak * 1e12), alg_bytes / (float(peaks["hbm_gbs"]) * 1e9)) * 1e6,
+                "algorithmic_flops": flops,
+                "algorithmic_bytes": alg_bytes,
+            },
+            "cpu_baseline": cpu,
+            "e2e": {"value": job_throughput(w0.n_rows * args.steps, world, t_e2e), "unit": UNIT,
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clocks,
+        }
+    barrier(world)
+    return result
+
+
+# ---------------------------------------------------------------------------------------
+# CPU oracle (baseline leg and the reference arm)
+# ---------------------------------------------------------------------------------------
+
+class OracleStep:
+    """The oracle's pass over sampled rows of one batch: append of their new tokens + decode."""
+
+    def __init__(self, w: synth.DecodeWorkload, rows: np.ndarray):
+        import oracle
+        self.oracle = oracle
+        slots, q, idx = synth.compact_for_rows(w, rows)
+        lat, rope = synth.pool_rows(w.pool_seed, torch.from_numpy(slots))
+        self.cache = np.zeros((slots.size + rows.size, w.record_bytes), dtype=np.uint8)
+        oracle.quantize_append(synth.bf16_bits(lat), synth.bf16_bits(rope), np.arange(slots.size), self.cache)
+        self.q = synth.bf16_bits(q)
+        self.idx = idx
+        self.w = w
+        nl, nr, _ = new_token_batch(w, 0)
+        self.new_lat = synth.bf16_bits(nl)[: rows.size]
+        self.new_rope = synth.bf16_bits(nr)[: rows.size]
+        self.new_slots = np.arange(slots.size, slots.size + rows.size, dtype=np.int64)
+        self.rows = rows.size
+
+    def __call__(self):
+        self.oracle.quantize_append(self.new_lat, self.new_rope, self.new_slots, self.cache)
+        self.oracle.sparse_mla_decode(self.q, self.cache, self.idx, self.w.sm_scale)
+        return self.rows
+
+
+def cpu_baseline(args, w):
+    import oracle
+    rows = np.arange(w.n_rows)
+    job = OracleStep(w, rows)
+    t0 = time.perf_counter()
+    done, reps = 0, 0
+    while True:
+        done += job()
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= args.cpu_seconds or reps >= 50:
+            break
+    return {"value": done / el, "unit": UNIT, "cores": oracle.threads_available(), "kind": "oracle",
+            "sample": f"{reps} x one full step ({w.n_rows} rows x {w.h_q} heads x {w.topk} keys, plus the "
+                      f"{w.n_rows} appended tokens), fp64 C oracle, OpenMP over heads",
+            "seconds": el}
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return None
+    import oracle
+    sets = make_sets(seed=0)
+    w0 = sets[0]
+    per_step = args.ref_rows
+    jobs = [OracleStep(s, np.arange(k * per_step, (k + 1) * per_step) % s.n_rows) for k, s in enumerate(sets)]
+    for k in range(args.warmup):
+        jobs[k % N_SETS]()
+    t0 = time.perf_counter()
+    done = 0
+    for k in range(args.steps):
+        done += jobs[k % N_SETS]()
+    el = time.perf_counter() - t0
+    value = done / el
+    return {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": value,
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": el / args.steps * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": w0.name, "batch": w0.B, "s_q": w0.s_q, "h_q": w0.h_q, "topk": w0.topk,
+                   "record_bytes": w0.record_bytes, "pool_slots": w0.num_slots,
+                   "rows_per_step": per_step},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.threads_available(), "kind": "oracle",
+                         "sample": f"{per_step} of {w0.n_rows} query rows per step (all heads, all keys) "
+                                   f"plus their appended tokens"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["gpu", "reference"], default="gpu")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--ref-rows", type=int, default=4)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        res = run_reference(args)
+    else:
+        res = run_gpu(args)
+    if res is not None:
+        print(json.dumps(res), flush=True)
+    world, _, _ = dist_env()
+    if world > 1 and args.impl == "gpu":
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

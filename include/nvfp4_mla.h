@@ -1,0 +1,139 @@
+/*
+ * nvfp4_mla.h -- C ABI of the NVFP4 MLA KV-cache library for GB300 (sm_103a).
+ *
+ * Two operations, as the pages state the problem:
+ *
+ *  1. nvfp4_mla_quantize_append: quantize each token's 512-dim MLA latent (NoPE) and 64-dim
+ *     RoPE key into one self-describing record and scatter it to its cache slot.
+ *     - 352-byte "nvfp4.fp8rope" record: FlashMLA PR 18 "W4A16 DSA: NVFP4 KV cache format for
+ *       SM100 sparse decode", format block "nvfp4.fp8rope (352 B/token)": bytes [0,256) hold
+ *       512 e2m1 values two per byte, [256,320) 64 unscaled e4m3 RoPE values, [320,352) 32
+ *       e4m3 scales, one per 16 values, the scale of block s at byte 320 + 8*(s&3) + (s>>2).
+ *     - 432-byte "nvfp4_ds_mla" record: vLLM PR 82 "kv: nvfp4_ds_mla - 4-bit NVFP4 KV cache for
+ *       B12X sparse MLA (SM120)", Problem and Fix / Write side: 256 B e2m1 NoPE, 32 B e4m3
+ *       scales in block order, 16 zero bytes, 128 B bf16 RoPE copied verbatim.
+ *     - Scale rule (vLLM PR 82, Tests): scale = E4M3(group_amax / 6); values are rounded to
+ *       the nearest e2m1 grid point after division by the decoded scale.
+ *
+ *  2. nvfp4_sparse_mla_decode: DeepSeek-style sparse MLA decode over one shared latent KV
+ *     head: for each query row (b, i) and head h, the keys are the records its top-k index
+ *     list selects (FlashMLA PR 18, "Kernel:" paragraph: keys dequantized to bf16, QK^T over
+ *     576 = 512 NoPE + 64 RoPE dims, PV over the 512 NoPE dims, bf16 MMAs with fp32
+ *     accumulation, attention sink and invalid indices per its validation list).
+ *
+ * Conventions shared by every call
+ *  - All data pointers are DEVICE pointers unless stated; the caller owns every buffer.
+ *    The library keeps no state between calls and allocates no device memory.
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream). Work is enqueued on it
+ *    and the call returns without synchronizing.
+ *  - Every argument check runs on the host before any launch; a failed check returns a
+ *    status below and launches nothing. Kernels never trap: problems found on the device
+ *    are OR-ed into *dev_status (if non-NULL) as NVFP4_MLA_DEV_* bits, readable after the
+ *    stream has been synchronized.
+ *  - The library is built for sm_103a only; calls on any other device return
+ *    NVFP4_MLA_ERR_UNSUPPORTED.
+ */
+#ifndef NVFP4_MLA_H_
+#define NVFP4_MLA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define NVFP4_MLA_API __attribute__((visibility("default")))
+
+/* Return codes of every call. */
+typedef enum {
+    NVFP4_MLA_OK = 0,
+    NVFP4_MLA_ERR_INVALID_ARG = 1,   /* null pointer, bad size, stride or alignment      */
+    NVFP4_MLA_ERR_UNSUPPORTED = 2,   /* record width, head count or device not supported */
+    NVFP4_MLA_ERR_CUDA = 3,          /* a CUDA runtime call failed (launch, attribute)   */
+    NVFP4_MLA_ERR_WORKSPACE = 4      /* workspace missing, too small or misaligned        */
+} nvfp4_mla_status;
+
+/* Bits the kernels OR into *dev_status. */
+#define NVFP4_MLA_DEV_SLOT_OUT_OF_RANGE 0x1u  /* quantize_append: slot >= num_slots (skipped) */
+#define NVFP4_MLA_DEV_INDEX_OUT_OF_RANGE 0x2u /* decode: index >= num_slots (masked)          */
+#define NVFP4_MLA_DEV_TIMEOUT 0x4u            /* decode: a pipeline wait gave up; out invalid */
+
+/*
+ * Quantize-and-append (write side).
+ *   kv_latent          bf16 [num_tokens, 512], row stride latent_row_stride ELEMENTS, inner
+ *                      stride 1; base 16-byte aligned, latent_row_stride % 8 == 0.
+ *   k_rope             bf16 [num_tokens, 64], its own row stride rope_row_stride ELEMENTS
+ *                      (may differ from the latent's); base 16-byte aligned, stride % 8 == 0.
+ *   slot_mapping       int64 [num_tokens]: record slot of each token. A negative slot skips
+ *                      the token (padding); a slot >= num_slots is skipped and sets
+ *                      NVFP4_MLA_DEV_SLOT_OUT_OF_RANGE. Slots should be distinct; if two tokens
+ *                      share a slot, which record lands there is unspecified.
+ *   cache              uint8 [num_slots, record_bytes], 16-byte aligned. Only the slots named
+ *                      by slot_mapping are written; every other byte is left untouched.
+ *   record_bytes       352 or 432.
+ *   dev_status         nullable device uint32 (see NVFP4_MLA_DEV_*).
+ * num_tokens == 0 is valid and launches nothing.
+ */
+NVFP4_MLA_API int nvfp4_mla_quantize_append(const void* kv_latent, int64_t latent_row_stride,
+                                            const void* k_rope, int64_t rope_row_stride,
+                                            const int64_t* slot_mapping, int64_t num_tokens,
+                                            uint8_t* cache, int64_t num_slots, int32_t record_bytes,
+                                            uint32_t* dev_status, void* stream);
+
+/*
+ * Scratch size of nvfp4_sparse_mla_decode for a problem (host-only, no CUDA call).
+ *   num_splits: the top-k list of each query row is cut into num_splits consecutive parts
+ *   computed in parallel and merged by a second kernel; 0 lets the library choose from the
+ *   problem size and the SM count of the current device (then this call reads the device
+ *   attribute). The workspace holds fp32 partial outputs and log-sum-exps of every part;
+ *   it is 0 bytes when a single part is used.
+ * Returns NVFP4_MLA_OK and sets *bytes, or an error code for an invalid problem.
+ */
+NVFP4_MLA_API int nvfp4_sparse_mla_decode_workspace_size(int32_t batch, int32_t s_q, int32_t h_q,
+                                                         int32_t topk, int32_t record_bytes,
+                                                         int32_t num_splits, size_t* bytes);
+
+/*
+ * Sparse MLA decode (read side).
+ *   q            bf16 [batch, s_q, h_q, 576], contiguous, 16-byte aligned. Dims [0,512) are
+ *                the NoPE (latent) part, [512,576) the RoPE part.
+ *   cache        uint8 [num_slots, record_bytes], 16-byte aligned, as written by
+ *                nvfp4_mla_quantize_append.
+ *   indices      int32 [batch, s_q, topk], contiguous: the cache slots each query row attends.
+ *                An entry < 0 is masked (padding); an entry >= num_slots is masked and sets
+ *                NVFP4_MLA_DEV_INDEX_OUT_OF_RANGE. Repeated entries count once per occurrence.
+ *   h_q          64 or 128. topk >= 1 (any value; the tail tile is masked).
+ *   sm_scale     softmax scale applied to q.k (e.g. 1/sqrt(576)).
+ *   attn_sink    nullable fp32 [h_q]: per-head extra logit that enters the softmax
+ *                denominator of `out` only (no value vector) and not `lse`.
+ *   out          bf16 [batch, s_q, h_q, 512], contiguous, 16-byte aligned:
+ *                out = sum_j e^{z_j} V_j / (sum_j e^{z_j} + e^{sink_h}), z_j = sm_scale q.K_j
+ *   lse          fp32 [batch, s_q, h_q]: natural-log log-sum-exp of the z_j of the used
+ *                entries (sink excluded). A row with no used entry gets out = 0, lse = -inf.
+ *   num_splits   0 = library choice, else 1..64 (see ..._workspace_size).
+ *   workspace    device scratch of at least the size ..._workspace_size reports for the same
+ *                arguments, 256-byte aligned; may be NULL when that size is 0.
+ *   dev_status   nullable device uint32 (see NVFP4_MLA_DEV_*).
+ * Precision: dequantized keys are exact in bf16; the two contractions run on tcgen05 bf16
+ * MMAs with fp32 accumulation; softmax in fp32; `out` is rounded to bf16 once.
+ */
+NVFP4_MLA_API int nvfp4_sparse_mla_decode(const void* q, const uint8_t* cache, int64_t num_slots,
+                                          int32_t record_bytes, const int32_t* indices,
+                                          int32_t batch, int32_t s_q, int32_t h_q, int32_t topk,
+                                          float sm_scale, const float* attn_sink, void* out,
+                                          float* lse, int32_t num_splits, void* workspace,
+                                          size_t workspace_bytes, uint32_t* dev_status,
+                                          void* stream);
+
+/* Static text for a status code (never NULL). */
+NVFP4_MLA_API const char* nvfp4_mla_status_string(int status);
+
+/* Library version as 10000*major + 100*minor + patch. */
+NVFP4_MLA_API int nvfp4_mla_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NVFP4_MLA_H_ */

@@ -1,0 +1,161 @@
+"""Python binding of the NVFP4 MLA KV-cache library (``include/nvfp4_mla.h``).
+
+Argument marshalling only: every step of the computation runs in the CUDA library
+``_build/libnvfp4mla.so`` (built by ``build.py``). PyTorch provides device memory and the
+current stream. There is no fallback: if the library is missing or the device is not
+sm_103, the calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Tuple
+
+import torch
+
+from . import build as _build
+
+RECORD_BYTES = (352, 432)
+D_NOPE, D_ROPE, D_QK, D_V = 512, 64, 576, 512
+
+OK = 0
+ERR_INVALID_ARG = 1
+ERR_UNSUPPORTED = 2
+ERR_CUDA = 3
+ERR_WORKSPACE = 4
+DEV_SLOT_OUT_OF_RANGE = 0x1
+DEV_INDEX_OUT_OF_RANGE = 0x2
+DEV_TIMEOUT = 0x4
+
+EXPORTED = (
+    "nvfp4_mla_quantize_append",
+    "nvfp4_sparse_mla_decode_workspace_size",
+    "nvfp4_sparse_mla_decode",
+    "nvfp4_mla_status_string",
+    "nvfp4_mla_version",
+)
+
+_lib: Optional[ctypes.CDLL] = None
+
+
+class Nvfp4MlaError(RuntimeError):
+    def __init__(self, call: str, status: int):
+        self.status = status
+        super().__init__(f"{call} failed with status {status}: {status_string(status)}")
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = False) -> ctypes.CDLL:
+    """Load the in-tree library (raises if it is absent and build_if_missing is False)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = _build.LIB
+    if not os.path.exists(path):
+        if not build_if_missing:
+            raise ImportError(f"CUDA library not built: {path} (run __graft_entry__.build())")
+        _build.build()
+    lib = ctypes.CDLL(path)
+    P, i64, i32, f32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_float, ctypes.c_size_t
+    lib.nvfp4_mla_quantize_append.restype = ctypes.c_int
+    lib.nvfp4_mla_quantize_append.argtypes = [P, i64, P, i64, P, i64, P, i64, i32, P, P]
+    lib.nvfp4_sparse_mla_decode_workspace_size.restype = ctypes.c_int
+    lib.nvfp4_sparse_mla_decode_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32, ctypes.POINTER(sz)]
+    lib.nvfp4_sparse_mla_decode.restype = ctypes.c_int
+    lib.nvfp4_sparse_mla_decode.argtypes = [P, P, i64, i32, P, i32, i32, i32, i32, f32, P, P, P, i32, P, sz, P, P]
+    lib.nvfp4_mla_status_string.restype = ctypes.c_char_p
+    lib.nvfp4_mla_status_string.argtypes = [ctypes.c_int]
+    lib.nvfp4_mla_version.restype = ctypes.c_int
+    lib.nvfp4_mla_version.argtypes = []
+    _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load().nvfp4_mla_status_string(int(status)).decode()
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(call: str, status: int):
+    if status != OK:
+        raise Nvfp4MlaError(call, status)
+
+
+def _need(cond: bool, msg: str):
+    if not cond:
+        raise ValueError(msg)
+
+
+def quantize_append(kv_latent: torch.Tensor, k_rope: torch.Tensor, slot_mapping: torch.Tensor,
+                    cache: torch.Tensor, dev_status: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Quantize ``kv_latent`` (bf16 [T,512]) and ``k_rope`` (bf16 [T,64]) into records and
+    write them to ``cache`` (uint8 [num_slots, 352|432]) at ``slot_mapping`` (int64 [T])."""
+    _need(kv_latent.dtype == torch.bfloat16 and k_rope.dtype == torch.bfloat16, "inputs must be bf16")
+    _need(kv_latent.dim() == 2 and kv_latent.shape[1] == D_NOPE and kv_latent.stride(1) == 1, "kv_latent [T,512], inner stride 1")
+    _need(k_rope.dim() == 2 and k_rope.shape[1] == D_ROPE and k_rope.stride(1) == 1, "k_rope [T,64], inner stride 1")
+    T = kv_latent.shape[0]
+    _need(k_rope.shape[0] == T and slot_mapping.numel() == T, "token counts differ")
+    _need(slot_mapping.dtype == torch.int64 and slot_mapping.is_contiguous(), "slot_mapping int64 contiguous")
+    _need(cache.dtype == torch.uint8 and cache.dim() == 2 and cache.is_contiguous(), "cache uint8 [num_slots, R] contiguous")
+    _need(cache.shape[1] in RECORD_BYTES, "record width must be 352 or 432")
+    for t in (kv_latent, k_rope, slot_mapping, cache):
+        _need(t.is_cuda and t.device == cache.device, "all tensors on the same CUDA device")
+    st = load().nvfp4_mla_quantize_append(
+        _ptr(kv_latent), kv_latent.stride(0), _ptr(k_rope), k_rope.stride(0), _ptr(slot_mapping), T,
+        _ptr(cache), cache.shape[0], cache.shape[1], _ptr(dev_status), _stream(stream))
+    _check("nvfp4_mla_quantize_append", st)
+
+
+def workspace_size(batch: int, s_q: int, h_q: int, topk: int, record_bytes: int, num_splits: int = 0) -> int:
+    n = ctypes.c_size_t(0)
+    st = load().nvfp4_sparse_mla_decode_workspace_size(batch, s_q, h_q, topk, record_bytes, num_splits, ctypes.byref(n))
+    _check("nvfp4_sparse_mla_decode_workspace_size", st)
+    return int(n.value)
+
+
+def sparse_mla_decode(q: torch.Tensor, cache: torch.Tensor, indices: torch.Tensor, sm_scale: float,
+                      attn_sink: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
+                      lse: Optional[torch.Tensor] = None, num_splits: int = 0,
+                      workspace: Optional[torch.Tensor] = None, dev_status: Optional[torch.Tensor] = None,
+                      stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """q bf16 [B, s_q, h_q, 576], cache uint8 [N, 352|432], indices int32 [B, s_q, topk].
+    Returns (out bf16 [B, s_q, h_q, 512], lse fp32 [B, s_q, h_q])."""
+    _need(q.dtype == torch.bfloat16 and q.dim() == 4 and q.shape[3] == D_QK and q.is_contiguous(), "q bf16 [B,s_q,h_q,576] contiguous")
+    B, s_q, h_q, _ = q.shape
+    _need(indices.dtype == torch.int32 and indices.dim() == 3 and tuple(indices.shape[:2]) == (B, s_q)
+          and indices.is_contiguous(), "indices int32 [B,s_q,topk] contiguous")
+    topk = indices.shape[2]
+    _need(cache.dtype == torch.uint8 and cache.dim() == 2 and cache.is_contiguous() and cache.shape[1] in RECORD_BYTES,
+          "cache uint8 [N, 352|432] contiguous")
+    if attn_sink is not None:
+        _need(attn_sink.dtype == torch.float32 and attn_sink.numel() == h_q and attn_sink.is_contiguous(), "attn_sink fp32 [h_q]")
+    if out is None:
+        out = torch.empty((B, s_q, h_q, D_V), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, s_q, h_q), dtype=torch.float32, device=q.device)
+    _need(out.dtype == torch.bfloat16 and out.is_contiguous() and tuple(out.shape) == (B, s_q, h_q, D_V), "out bf16 [B,s_q,h_q,512]")
+    _need(lse.dtype == torch.float32 and lse.is_contiguous() and tuple(lse.shape) == (B, s_q, h_q), "lse fp32 [B,s_q,h_q]")
+    for t in (q, cache, indices, out, lse) + ((attn_sink,) if attn_sink is not None else ()):
+        _need(t.is_cuda and t.device == q.device, "all tensors on the same CUDA device")
+    need = workspace_size(B, s_q, h_q, topk, cache.shape[1], num_splits)
+    if need and (workspace is None or workspace.numel() * workspace.element_size() < need):
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = load().nvfp4_sparse_mla_decode(
+        _ptr(q), _ptr(cache), cache.shape[0], cache.shape[1], _ptr(indices), B, s_q, h_q, topk, float(sm_scale),
+        _ptr(attn_sink), _ptr(out), _ptr(lse), int(num_splits), _ptr(workspace), wbytes, _ptr(dev_status),
+        _stream(stream))
+    _check("nvfp4_sparse_mla_decode", st)
+    return out, lse

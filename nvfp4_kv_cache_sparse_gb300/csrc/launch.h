@@ -1,0 +1,39 @@
+// launch.h -- host-side launchers shared between the kernel translation units and the C ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+namespace nvfp4mla {
+
+cudaError_t launch_quantize_append(const void* kv_latent, int64_t latent_row_stride, const void* k_rope,
+                                   int64_t rope_row_stride, const int64_t* slot_mapping, int64_t num_tokens,
+                                   uint8_t* cache, int64_t num_slots, int record_bytes, uint32_t* dev_status,
+                                   int sm_count, cudaStream_t stream);
+
+struct DecodeArgs {
+    const void* q;             // bf16 [rows, h_q, 576]
+    const uint8_t* cache;      // [num_slots, record_bytes]
+    int64_t num_slots;
+    int record_bytes;
+    const int32_t* indices;    // [rows, topk]
+    int rows;                  // batch * s_q
+    int h_q;
+    int topk;
+    float sm_scale;
+    const float* attn_sink;    // nullable [h_q]
+    void* out;                 // bf16 [rows, h_q, 512]
+    float* lse;                // [rows, h_q]
+    int splits;
+    float* part_out;           // fp32 [rows, splits, h_q, 512] when splits > 1
+    float* part_lse;           // fp32 [rows, splits, h_q]
+    uint32_t* dev_status;
+};
+
+// Keys of one split, rounded to whole tiles.
+int decode_keys_per_split(int topk, int splits);
+cudaError_t launch_sparse_decode(const DecodeArgs& a, cudaStream_t stream);
+
+}  // namespace nvfp4mla

@@ -1,0 +1,164 @@
+// quantize_append.cu -- write side: quantize each token's 512 bf16 NoPE values and 64 bf16
+// RoPE values into one NVFP4 record and scatter it to its cache slot.
+//
+// Record formats:
+//  * 352 B, FlashMLA PR 18 "W4A16 DSA: NVFP4 KV cache format for SM100 sparse decode",
+//    format block "nvfp4.fp8rope (352 B/token)": [0,256) e2m1 pairs, [256,320) unscaled e4m3
+//    RoPE, [320,352) e4m3 scales with block s at byte 320 + 8*(s&3) + (s>>2).
+//  * 432 B, vLLM PR 82 "kv: nvfp4_ds_mla - 4-bit NVFP4 KV cache for B12X sparse MLA (SM120)",
+//    Problem / Fix (Write side): [0,256) e2m1 pairs, [256,288) scales in block order,
+//    [288,304) zeros, [304,432) bf16 RoPE copied verbatim.
+// Scale rule (vLLM PR 82, Tests): scale = E4M3(group_amax / 6), round-to-nearest-even and
+// saturating; each value is rounded to the nearest e2m1 grid point (ties to even, saturating)
+// after division by the decoded scale; the sign of the input is always kept.
+//
+// Design: one warp per token, lane g owns the 16-value group g. The group maximum is taken on
+// the |bf16| bit patterns (non-negative floats order like integers), so no shuffles are
+// needed. The record is assembled in a per-warp shared-memory stage and written with 16-byte
+// stores (22 lanes for 352 B, 27 for 432 B), so each record is one contiguous burst.
+//
+// Exactness of x / s without a division per value: s is an e4m3 value (<= 4 significant bits)
+// and x a bf16 value (<= 8), so the exact quotient x/s is either exactly one of the e2m1 tie
+// points {0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5} or at least 1/300 (relative) away from all of
+// them. q = |x| * rn(1/s) is within 2^-23 (relative) of x/s; rounding q to 12 significant bits
+// therefore lands exactly on the tie point in the first case and cannot cross one in the
+// second, so the hardware e2m1 rounding of that value equals the rounding of the IEEE
+// quotient. amax / 6 uses a correctly rounded division (one per group).
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "launch.h"
+
+namespace nvfp4mla {
+namespace {
+
+constexpr int kWarpsPerBlock = 8;
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// e4m3 codes of two non-negative floats, round-to-nearest-even, saturating:
+// bits [15:8] = code(hi), [7:0] = code(lo).
+__device__ __forceinline__ uint32_t e4m3x2_rn_sat(float hi, float lo) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// e2m1 codes of two non-negative floats, round-to-nearest-even, saturating:
+// bits [7:4] = code(hi), [3:0] = code(lo).
+__device__ __forceinline__ uint32_t e2m1x2_rn_sat(float hi, float lo) {
+    uint32_t r;
+    asm("{\n"
+        "  .reg .b8 t;\n"
+        "  cvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n"
+        "  cvt.u32.u8 %0, t;\n"
+        "}\n"
+        : "=r"(r)
+        : "f"(hi), "f"(lo));
+    return r;
+}
+
+// Value of a non-negative finite e4m3 code (0x00..0x7E), built from its bit fields.
+__device__ __forceinline__ float e4m3_code_value(uint32_t c) {
+    const uint32_t e = c >> 3, m = c & 7u;
+    return e ? __uint_as_float(((e + 120u) << 23) | (m << 20)) : static_cast<float>(m) * 0.001953125f;
+}
+
+// Round a non-negative float to 12 significant bits (see the file comment).
+__device__ __forceinline__ float round_to_12_bits(float v) {
+    return __uint_as_float((__float_as_uint(v) + 0x800u) & ~0xFFFu);
+}
+
+template <int R>
+__global__ void __launch_bounds__(kWarpsPerBlock * 32)
+quantize_append_kernel(const uint16_t* __restrict__ latent, int64_t latent_stride, const uint16_t* __restrict__ rope,
+                       int64_t rope_stride, const int64_t* __restrict__ slot_mapping, int64_t num_tokens,
+                       uint8_t* __restrict__ cache, int64_t num_slots, uint32_t* __restrict__ dev_status) {
+    __shared__ __align__(16) uint8_t stage[kWarpsPerBlock][R];
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    uint8_t* rec = stage[warp];
+
+    for (int64_t t = static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + warp; t < num_tokens;
+         t += static_cast<int64_t>(gridDim.x) * kWarpsPerBlock) {
+        const int64_t slot = __ldg(slot_mapping + t);
+        if (slot < 0) continue;
+        if (slot >= num_slots) {
+            if (lane == 0 && dev_status != nullptr) atomicOr(dev_status, 0x1u);
+            continue;
+        }
+
+        // ---- NoPE group `lane`: 16 bf16 values = two 16-byte loads
+        const uint4* src = reinterpret_cast<const uint4*>(latent + t * latent_stride) + 2 * lane;
+        const uint4 va = __ldg(src);
+        const uint4 vb = __ldg(src + 1);
+        const uint32_t w[8] = {va.x, va.y, va.z, va.w, vb.x, vb.y, vb.z, vb.w};
+        uint32_t amax_bits = 0;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            amax_bits = max(amax_bits, max(w[k] & 0x7FFFu, (w[k] >> 16) & 0x7FFFu));
+        }
+        const float amax = __uint_as_float(amax_bits << 16);
+        const uint32_t sbyte = e4m3x2_rn_sat(0.0f, __fdiv_rn(amax, 6.0f)) & 0xFFu;
+        const float inv_s = sbyte ? __frcp_rn(e4m3_code_value(sbyte)) : 0.0f;
+
+        uint32_t packed[2] = {0u, 0u};
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const float q0 = round_to_12_bits(fabsf(bf16_lo(w[k])) * inv_s);
+            const float q1 = round_to_12_bits(fabsf(bf16_hi(w[k])) * inv_s);
+            uint32_t byte = e2m1x2_rn_sat(q1, q0);                    // even element -> low nibble
+            byte |= ((w[k] >> 12) & 0x8u) | ((w[k] >> 24) & 0x80u);   // signs of both elements
+            packed[k >> 2] |= byte << (8 * (k & 3));
+        }
+        *reinterpret_cast<uint2*>(rec + 8 * lane) = make_uint2(packed[0], packed[1]);
+
+        // ---- RoPE: lane owns elements 2*lane and 2*lane+1
+        const uint32_t rw = __ldg(reinterpret_cast<const uint32_t*>(rope + t * rope_stride) + lane);
+        if constexpr (R == 352) {
+            rec[320 + 8 * (lane & 3) + (lane >> 2)] = static_cast<uint8_t>(sbyte);
+            uint32_t c = e4m3x2_rn_sat(fabsf(bf16_hi(rw)), fabsf(bf16_lo(rw)));
+            c |= ((rw >> 8) & 0x80u) | ((rw >> 16) & 0x8000u);
+            *reinterpret_cast<uint16_t*>(rec + 256 + 2 * lane) = static_cast<uint16_t>(c);
+        } else {
+            rec[256 + lane] = static_cast<uint8_t>(sbyte);
+            *reinterpret_cast<uint32_t*>(rec + 304 + 4 * lane) = rw;
+            if (lane < 4) *reinterpret_cast<uint32_t*>(rec + 288 + 4 * lane) = 0u;
+        }
+        __syncwarp();
+        if (lane < R / 16) {
+            const uint4 v = reinterpret_cast<const uint4*>(rec)[lane];
+            reinterpret_cast<uint4*>(cache + slot * R)[lane] = v;
+        }
+        __syncwarp();
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_quantize_append(const void* kv_latent, int64_t latent_row_stride, const void* k_rope,
+                                   int64_t rope_row_stride, const int64_t* slot_mapping, int64_t num_tokens,
+                                   uint8_t* cache, int64_t num_slots, int record_bytes, uint32_t* dev_status,
+                                   int sm_count, cudaStream_t stream) {
+    const int64_t want = (num_tokens + kWarpsPerBlock - 1) / kWarpsPerBlock;
+    const int64_t cap = static_cast<int64_t>(sm_count) * 8;   // 8 blocks of 256 threads per SM
+    const int grid = static_cast<int>(want < cap ? want : cap);
+    const dim3 block(kWarpsPerBlock * 32);
+    const auto* lat = static_cast<const uint16_t*>(kv_latent);
+    const auto* rope = static_cast<const uint16_t*>(k_rope);
+    if (record_bytes == 352) {
+        quantize_append_kernel<352><<<grid, block, 0, stream>>>(lat, latent_row_stride, rope, rope_row_stride,
+                                                                slot_mapping, num_tokens, cache, num_slots,
+                                                                dev_status);
+    } else {
+        quantize_append_kernel<432><<<grid, block, 0, stream>>>(lat, latent_row_stride, rope, rope_row_stride,
+                                                                slot_mapping, num_tokens, cache, num_slots,
+                                                                dev_status);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace nvfp4mla

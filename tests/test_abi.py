@@ -1,0 +1,64 @@
+"""The C-ABI library builds, loads and exports every symbol include/nvfp4_mla.h declares;
+argument checks that need no device return their status codes. No kernel runs here."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import nvfp4_kv_cache_sparse_gb300 as lib
+from nvfp4_kv_cache_sparse_gb300 import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "nvfp4_mla.h")
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return re.findall(r"NVFP4_MLA_API\s+[\w\s\*]+?\b(nvfp4_\w+)\s*\(", text)
+
+
+@pytest.fixture(scope="module")
+def cdll():
+    build.build()
+    return lib.load()
+
+
+def test_header_declares_the_expected_calls():
+    syms = declared_symbols()
+    assert set(syms) == set(lib.EXPORTED), syms
+
+
+def test_library_exports_every_declared_symbol(cdll):
+    for name in declared_symbols():
+        assert hasattr(cdll, name), name
+    nm = os.popen(f"nm -D --defined-only {build.LIB}").read()
+    exported = set(re.findall(r"\bT (nvfp4_\w+)", nm))
+    assert exported == set(declared_symbols())
+
+
+def test_status_strings_and_version(cdll):
+    for code in range(5):
+        assert isinstance(lib.status_string(code), str) and lib.status_string(code)
+    assert lib.status_string(99) == "unknown status"
+    assert cdll.nvfp4_mla_version() == 100
+
+
+def test_host_side_checks_return_codes_without_a_device(cdll):
+    # unsupported record width / head count are rejected before any CUDA call
+    n = ctypes.c_size_t(123)
+    assert cdll.nvfp4_sparse_mla_decode_workspace_size(1, 1, 64, 64, 400, 1, ctypes.byref(n)) == lib.ERR_UNSUPPORTED
+    assert cdll.nvfp4_sparse_mla_decode_workspace_size(1, 1, 96, 64, 352, 1, ctypes.byref(n)) == lib.ERR_UNSUPPORTED
+    assert cdll.nvfp4_sparse_mla_decode_workspace_size(1, 1, 64, 0, 352, 1, ctypes.byref(n)) == lib.ERR_INVALID_ARG
+    assert cdll.nvfp4_sparse_mla_decode_workspace_size(1, 1, 64, 64, 352, 65, ctypes.byref(n)) == lib.ERR_INVALID_ARG
+    # an explicit split count needs no device: workspace = partial outputs + lse (256-B padded)
+    assert cdll.nvfp4_sparse_mla_decode_workspace_size(2, 1, 64, 64, 352, 1, ctypes.byref(n)) == lib.OK and n.value == 0
+    assert cdll.nvfp4_sparse_mla_decode_workspace_size(2, 1, 64, 64, 352, 2, ctypes.byref(n)) == lib.OK
+    assert n.value == 2 * 2 * 64 * 512 * 4 + 1024
+    # quantize_append: zero tokens is a no-op; bad record width / null pointers are errors
+    assert cdll.nvfp4_mla_quantize_append(None, 512, None, 64, None, 0, None, 0, 352, None, None) == lib.OK
+    assert cdll.nvfp4_mla_quantize_append(None, 512, None, 64, None, 4, None, 8, 352, None, None) == lib.ERR_INVALID_ARG
+    assert cdll.nvfp4_mla_quantize_append(None, 512, None, 64, None, 4, None, 8, 353, None, None) == lib.ERR_UNSUPPORTED
+    # decode: null pointers
+    assert cdll.nvfp4_sparse_mla_decode(None, None, 8, 352, None, 1, 1, 64, 64, 1.0, None, None, None, 1, None, 0,
+                                        None, None) == lib.ERR_INVALID_ARG
