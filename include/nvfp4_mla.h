@@ -23,7 +23,8 @@
  *
  * Conventions shared by every call
  *  - All data pointers are DEVICE pointers unless stated; the caller owns every buffer.
- *    The library keeps no state between calls and allocates no device memory.
+ *    No call allocates device memory. The only device memory the library owns is the
+ *    fixed scratch array of nvfp4_sparse_mla_decode_no_alloc (see there).
  *  - `stream` is a cudaStream_t (NULL = the legacy default stream). Work is enqueued on it
  *    and the call returns without synchronizing.
  *  - Every argument check runs on the host before any launch; a failed check returns a
@@ -125,6 +126,36 @@ NVFP4_MLA_API int nvfp4_sparse_mla_decode(const void* q, const uint8_t* cache, i
                                           float* lse, int32_t num_splits, void* workspace,
                                           size_t workspace_bytes, uint32_t* dev_status,
                                           void* stream);
+
+/*
+ * Sparse MLA decode for callers that cannot allocate device memory. (The pages have no
+ * counterpart to this call; it is a service of this library.)
+ *
+ * nvfp4_sparse_mla_decode needs a caller-provided workspace when it splits the top-k lists.
+ * Some callers cannot provide one: code that works within a device-memory budget fixed at
+ * start-up and may not call cudaMalloc afterwards, code that must avoid cudaMalloc/cudaFree
+ * because they can synchronize the device, or a host that lends the library only its input
+ * and output buffers. This call takes the same arguments as nvfp4_sparse_mla_decode without
+ * the workspace, and keeps its scratch in a library-owned, fixed-size device array of
+ * NVFP4_MLA_NO_ALLOC_SCRATCH_BYTES bytes (reserved on every GPU that loads the library until
+ * the process exits). It calls no cudaMalloc, cudaFree or allocating routine.
+ *  - A problem whose split count (num_splits, or the library's choice when 0) needs more
+ *    scratch than that returns NVFP4_MLA_ERR_WORKSPACE and launches nothing; pass a smaller
+ *    num_splits (1 needs no scratch).
+ *  - The first call on each device looks up the array's device address with that device
+ *    current and caches it; make that first call before any stream capture.
+ *  - All calls share the array and it keeps the last call's contents (nothing in it needs to
+ *    start at zero: each call writes every value it reads). Calls whose kernels may overlap on
+ *    the GPU, e.g. on unordered streams, race on it and must be serialized by the caller.
+ * Results equal those of nvfp4_sparse_mla_decode with the same num_splits.
+ */
+#define NVFP4_MLA_NO_ALLOC_SCRATCH_BYTES (((size_t)32) << 20)
+
+NVFP4_MLA_API int nvfp4_sparse_mla_decode_no_alloc(const void* q, const uint8_t* cache, int64_t num_slots,
+                                                   int32_t record_bytes, const int32_t* indices, int32_t batch,
+                                                   int32_t s_q, int32_t h_q, int32_t topk, float sm_scale,
+                                                   const float* attn_sink, void* out, float* lse,
+                                                   int32_t num_splits, uint32_t* dev_status, void* stream);
 
 /* Static text for a status code (never NULL). */
 NVFP4_MLA_API const char* nvfp4_mla_status_string(int status);

@@ -31,6 +31,7 @@ EXPORTED = (
     "nvfp4_mla_quantize_append",
     "nvfp4_sparse_mla_decode_workspace_size",
     "nvfp4_sparse_mla_decode",
+    "nvfp4_sparse_mla_decode_no_alloc",
     "nvfp4_mla_status_string",
     "nvfp4_mla_version",
 )
@@ -66,6 +67,8 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
     lib.nvfp4_sparse_mla_decode_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32, ctypes.POINTER(sz)]
     lib.nvfp4_sparse_mla_decode.restype = ctypes.c_int
     lib.nvfp4_sparse_mla_decode.argtypes = [P, P, i64, i32, P, i32, i32, i32, i32, f32, P, P, P, i32, P, sz, P, P]
+    lib.nvfp4_sparse_mla_decode_no_alloc.restype = ctypes.c_int
+    lib.nvfp4_sparse_mla_decode_no_alloc.argtypes = [P, P, i64, i32, P, i32, i32, i32, i32, f32, P, P, P, i32, P, P]
     lib.nvfp4_mla_status_string.restype = ctypes.c_char_p
     lib.nvfp4_mla_status_string.argtypes = [ctypes.c_int]
     lib.nvfp4_mla_version.restype = ctypes.c_int
