@@ -12,7 +12,7 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 constexpr int kMaxSplits = 64;
-constexpr int kDecodeTile = 32;
+constexpr int kDecodeTile = 64;
 
 // Per-device cache of (arch ok, SM count); 0 = unknown.
 std::atomic<int> g_dev_state[kMaxDevices];   // -1 unsupported, >0 SM count

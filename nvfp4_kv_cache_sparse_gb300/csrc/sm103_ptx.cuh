@@ -198,3 +198,153 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
 }
 
 }  // namespace nvfp4mla
+
+namespace nvfp4mla {
+
+// ---------------------------------------------------------------------------------------
+// Thread-block clusters and distributed shared memory
+// ---------------------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Address, in the shared::cluster window, of the same byte in CTA `rank`'s shared memory.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t local_saddr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local_saddr), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ void st_cluster_v4(uint32_t cluster_saddr, float a, float b, float c, float d) {
+    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(cluster_saddr), "f"(a), "f"(b), "f"(c),
+                 "f"(d)
+                 : "memory");
+}
+
+// Arrive (release at cluster scope) on an mbarrier given by its shared::cluster address.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_saddr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_saddr) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n"
+        "  .reg .pred p;\n"
+        "  mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+        "  selp.u32 %0, 1, 0, p;\n"
+        "}\n"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait with cluster-scope acquire (for barriers that a peer CTA arrives on).
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, uint32_t limit = (1u << 20)) {
+    for (uint32_t i = 0; i < limit; ++i) {
+        if (mbar_try_wait_cluster(bar, parity)) return true;
+    }
+    return false;
+}
+
+// Whole-cluster barrier (every thread of every CTA of the cluster).
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32_wait(uint32_t taddr, uint32_t (&r)[32]) {
+    tmem_ld32(taddr, r);
+    tmem_wait_ld();
+}
+
+}  // namespace nvfp4mla
+
+namespace nvfp4mla {
+
+// Asynchronous 16-byte store into a peer CTA's shared memory; completion is counted as 16
+// transaction bytes on the peer's mbarrier (both addresses in the shared::cluster window).
+__device__ __forceinline__ void st_async_v4(uint32_t cluster_saddr, float a, float b, float c, float d,
+                                            uint32_t cluster_mbar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                     cluster_saddr),
+                 "f"(a), "f"(b), "f"(c), "f"(d), "r"(cluster_mbar)
+                 : "memory");
+}
+
+// Arrive on a local mbarrier and add `bytes` to the transaction count its phase waits for.
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
+
+// 2^x, hardware approximation (relative error ~2^-22), denormal results flushed.
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+}  // namespace nvfp4mla
+
+namespace nvfp4mla {
+
+// Arrive on a peer CTA's mbarrier without memory ordering (a pure signal).
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_saddr) {
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_saddr) : "memory");
+}
+
+}  // namespace nvfp4mla
+
+namespace nvfp4mla {
+
+// tcgen05.commit whose arrival goes to the mbarrier at the same shared-memory offset in every
+// CTA of the cluster named by `cta_mask`.
+__device__ __forceinline__ void mma_commit_multicast(uint64_t* bar, uint16_t cta_mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            smem_addr(bar)),
+        "h"(cta_mask)
+        : "memory");
+}
+
+__device__ __forceinline__ void st_async_f32(uint32_t cluster_saddr, float a, uint32_t cluster_mbar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.f32 [%0], %1, [%2];" ::"r"(cluster_saddr),
+                 "f"(a), "r"(cluster_mbar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void st_async_v2(uint32_t cluster_saddr, float a, float b, uint32_t cluster_mbar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];" ::"r"(
+                     cluster_saddr),
+                 "f"(a), "f"(b), "r"(cluster_mbar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void st_async_u4(uint32_t cluster_saddr, uint4 v, uint32_t cluster_mbar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                     cluster_saddr),
+                 "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(cluster_mbar)
+                 : "memory");
+}
+
+}  // namespace nvfp4mla
+
+namespace nvfp4mla {
+
+// 16-byte global -> shared copy that bypasses L1 and completes asynchronously (commit groups).
+__device__ __forceinline__ void cp_async16(uint32_t saddr, const void* gptr) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(saddr), "l"(gptr) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+}  // namespace nvfp4mla

@@ -7,22 +7,25 @@
 //     out = sum_j e^{z_j} V_j / (sum_j e^{z_j} + e^{sink_h}),   V_j = K_j[0:512]
 //     lse = ln sum_j e^{z_j}
 // Keys are dequantized to bf16 in shared memory (exact: e2m1 x e4m3 has <= 5 significant
-// bits), both contractions run as tcgen05 bf16 MMAs with fp32 accumulation in tensor memory.
+// bits); both contractions run as tcgen05 bf16 MMAs with fp32 accumulation in tensor memory.
 //
-// Kernel organisation (one CTA per (query row, top-k split, half of the 512 value dims)):
-//   warps 0-3  softmax: thread r owns head r = TMEM lane r. Reads S = Q K^T from TMEM, keeps
-//              the running max/sum, writes P (bf16) back into TMEM over S, rescales O when
-//              the reference max moves, and writes the result.
-//   warps 4-7  gather/dequant: 4 threads per key, 32 keys per tile; each thread loads its
-//              part of the record with 8/16-byte loads and writes bf16 rows into a
-//              128-byte-swizzled K-major tile (the same bytes serve as the MN-major V tile).
-//   warp 8     TMEM allocation and MMA issue (one elected lane):
-//              QK: S[128 x 32]  = Q[128 x 576] (smem) * K_tile^T, 36 MMAs of K=16
-//              PV: O[128 x 256] += P[128 x 32] (TMEM) * V_tile[32 x 256] (smem), 2 MMAs
-// Heads are the MMA M dimension (h_q = 64 pads rows 64..127 with zeros). A full fp32 O of
-// 128 heads x 512 dims would fill all 512 TMEM columns, so each CTA owns 256 value dims and
-// both CTAs of a pair compute the same S (this duplicates QK; a later revision removes it).
-// TMEM columns: O [0,256), S/P double buffer [256,288) and [288,320).
+// Work split: a cluster of two CTAs per (query row, top-k split), with different roles.
+// With 128 heads, the fp32 accumulator O [128 x 512] fills all 512 TMEM columns of an SM, so
+// QK^T and PV run on different SMs and only the bf16 P tile travels between them:
+//   CTA 0 (QK): gathers whole records, dequantizes K tiles (576 dims), keeps Q [128 x 576]
+//     in TMEM as the MMA A operand, computes S = Q K^T, runs the online softmax, and sends
+//     each row's P (bf16) and rescale factor to CTA 1 with st.async (DSMEM, one way:
+//     132 B per head per 64 keys).
+//   CTA 1 (PV): gathers the NoPE half of the same records, dequantizes V tiles (512 dims),
+//     keeps O in TMEM and computes O += P V with P read from shared memory; its MMA commit
+//     multicasts back to CTA 0 to release the P slot. At the end CTA 0 sends each row's
+//     running max and sum, and CTA 1 normalizes and writes `out` (CTA 0 writes `lse`).
+// Warp roles (448 threads):
+//   CTA 0: warps 0-3 softmax (thread r = head r = TMEM lane r), 4-11 gather/dequant,
+//          12-13 QK issuers (even / odd tiles; one elected lane each).
+//   CTA 1: warps 0-3 rescale/epilogue (thread r = TMEM lane r), 4-11 gather/dequant, 12 PV issuer.
+// Tiles are 64 keys; every K/V tile is written in a 128B-swizzled layout that is the K-major
+// B operand of QK (CTA 0) or the MN-major B operand of PV (CTA 1).
 //
 // Every wait is bounded: on timeout the CTA sets NVFP4_MLA_DEV_TIMEOUT, stops issuing work,
 // waits (bounded) for its MMAs to drain and frees its tensor memory before returning.
@@ -38,34 +41,81 @@
 namespace nvfp4mla {
 namespace {
 
-constexpr int kTile = 32;                         // keys per tile
-constexpr int kHeadsM = 128;                      // MMA M (heads, zero padded)
+constexpr int kTile = 64;                          // keys per tile
+constexpr int kHeadsM = 128;                       // MMA M (heads, zero padded)
 constexpr int kDqk = 576;
-constexpr int kDBlocks = kDqk / 64;               // 9 swizzle blocks of 64 bf16 along d
-constexpr int kQBytes = kHeadsM * kDqk * 2;       // 147456
-constexpr int kQBlockBytes = kHeadsM * 128;       // 16384: one 64-wide d block of Q
-constexpr int kKTileBytes = kTile * kDqk * 2;     // 36864
-constexpr int kKBlockBytes = kTile * 128;         // 4096: one 64-wide d block of a K tile
-constexpr int kOCols = 256;
-constexpr int kSCol = 256;                        // S/P buffers at columns 256 and 288
+constexpr int kBlkBytes = kTile * 128;             // one 64-wide d block of a tile: 8 KB
+constexpr int kKStages = 2;                        // CTA 0: K tiles of 9 blocks (8 NoPE + RoPE)
+constexpr int kKTileBytes = 9 * kBlkBytes;         // 72 KB
+constexpr int kVStages = 2;                        // CTA 1: V tiles of 8 blocks
+constexpr int kVTileBytes = 8 * kBlkBytes;         // 64 KB
+constexpr int kPStages = 2;                        // CTA 1: P tiles [128 heads x 64 keys] bf16
+constexpr int kPBytes = kHeadsM * 128;             // 16 KB
+constexpr int kMaskSlots = 8;
+constexpr int kRawStages = 3;                      // raw records in flight (cp.async), in tiles
+// Raw record slot of one key: CTA 0 copies the whole record; CTA 1 the 256 NoPE bytes and the
+// 32 scale bytes (16-byte chunks 0..15 and 16..17 of the slot).
+template <int R, bool kWhole>
+struct RawSlot {
+    static constexpr int kChunks = kWhole ? R / 16 : 18;
+    static constexpr int kKeyBytes = kChunks * 16;
+    static constexpr int kTileBytes = kTile * kKeyBytes;
+    // record byte offset of slot chunk j
+    static __device__ __forceinline__ int src_offset(int j) {
+        return (kWhole || j < 16) ? 16 * j : (R == 352 ? 320 : 256) + 16 * (j - 16);
+    }
+    static constexpr int kScaleOffset = kWhole ? (R == 352 ? 320 : 256) : 256;
+};
+constexpr int kRaw0Bytes = kRawStages * kTile * 432;     // CTA 0 raw ring (largest record)
+constexpr int kRaw1Bytes = kRawStages * kTile * 288;     // CTA 1 raw ring
+constexpr uint32_t kColS = 0;                      // CTA 0: S buffers [0,64), [64,128)
+constexpr uint32_t kColQ = 128;                    // CTA 0: Q, 576 bf16 = 288 columns
+constexpr uint32_t kColO = 0;                      // CTA 1: O, 512 columns
 constexpr int kTmemCols = 512;
-constexpr int kThreads = 288;
+constexpr int kThreads = 448;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
-constexpr float kRescaleThreshold = 8.0f;         // log2 units: rescale O only when max grows by > 2^8
+constexpr float kRescaleThreshold = 8.0f;          // log2 units: rescale O only when max grows by > 2^8
 
+// Control block at the same offset in both CTAs (CTA 1's commits multicast into CTA 0's
+// pempty, and CTA 0's st.async completions land on CTA 1's pfull / fin).
 struct __align__(8) SmemCtl {
-    uint64_t kfull[2];
-    uint64_t kempty[2];
-    uint64_t sfull[2];
-    uint64_t pfull[2];
-    uint64_t odone[2];
+    // CTA 0
+    uint64_t kfull[kKStages];     // dequant -> QK issuer
+    uint64_t kempty[kKStages];    // QK commit -> dequant
+    uint64_t sfull[2];            // QK commit -> softmax
+    uint64_t sfree[2];            // softmax has read S -> QK issuer
+    uint64_t mfull[kMaskSlots];   // used-key mask of a tile written
+    uint64_t pempty[kPStages];    // CTA 1's PV has read the P slot (multicast commit)
+    uint64_t qready;              // Q in TMEM
+    // CTA 1
+    uint64_t vfull[kVStages];     // dequant -> PV issuer
+    uint64_t vempty[kVStages];    // PV commit -> dequant
+    uint64_t pfull[kPStages];     // P + alpha of a tile landed (tx-counted)
+    uint64_t ready[kPStages];     // epilogue warps checked alpha (and rescaled O) -> PV issuer
+    uint64_t odone[2];            // PV commit -> epilogue warps
+    uint64_t fin;                 // final (max, sum) of every row landed (tx-counted)
+    // both
     uint64_t drain;
     uint32_t tmem_base;
     uint32_t abort;
+    uint8_t mask[kMaskSlots][8];
 };
 
-constexpr int kSmemBytes = 1024 + kQBytes + 2 * kKTileBytes + 256;
+constexpr int kCtlBytes = 1024;
+static_assert(sizeof(SmemCtl) <= kCtlBytes, "control block");
+// CTA 0 data
+constexpr int kOffK = kCtlBytes;
+constexpr int kOffRaw0 = kOffK + kKStages * kKTileBytes;
+// CTA 1 data
+constexpr int kOffV = kCtlBytes;
+constexpr int kOffP = kOffV + kVStages * kVTileBytes;
+constexpr int kOffAlpha = kOffP + kPStages * kPBytes;          // [kPStages][128] fp32
+constexpr int kOffFin = kOffAlpha + kPStages * kHeadsM * 4;    // [128] (max, sum) pairs
+constexpr int kOffRaw1 = kOffFin + kHeadsM * 8;
+constexpr int kSmem0 = kOffRaw0 + kRaw0Bytes;
+constexpr int kSmem1 = kOffRaw1 + kRaw1Bytes;
+constexpr int kSmemBytes = 1024 + (kSmem0 > kSmem1 ? kSmem0 : kSmem1);
 
 struct KernelArgs {
     const uint16_t* q;
@@ -144,327 +194,532 @@ __device__ __forceinline__ void set_abort(SmemCtl* ctl, uint32_t* status) {
     if (atomicExch(&ctl->abort, 1u) == 0u && status != nullptr) atomicOr(status, 0x4u);
 }
 
+__device__ __forceinline__ bool aborted(SmemCtl* ctl) {
+    return *reinterpret_cast<volatile uint32_t*>(&ctl->abort) != 0u;
+}
+
 __device__ __forceinline__ bool wait_or_abort(SmemCtl* ctl, uint64_t* bar, uint32_t parity, uint32_t* status) {
-    if (*reinterpret_cast<volatile uint32_t*>(&ctl->abort)) return false;
+    if (aborted(ctl)) return false;
     if (mbar_wait(bar, parity)) return true;
     set_abort(ctl, status);
     return false;
 }
 
-// Same, with one answer for the whole warp (warps that go on to warp-collective tcgen05
-// instructions must take the same branch).
+// One answer for the whole warp (warps that go on to warp-collective instructions must take
+// the same branch).
 __device__ __forceinline__ bool wait_warp(SmemCtl* ctl, uint64_t* bar, uint32_t parity, uint32_t* status) {
     const bool ok = wait_or_abort(ctl, bar, parity, status);
     return __all_sync(0xffffffffu, ok);
 }
 
+// Index of this thread's key (or -1 past the end of the split).
+__device__ __forceinline__ int32_t load_index(const int32_t* idx_row, int pos, int key_end) {
+    return pos < key_end ? __ldg(idx_row + pos) : -1;
+}
+
+// Start the asynchronous copy of this thread's 16-byte chunks (j = q, q+4, ...) of one key's
+// raw record into its slot, or nothing for a masked key. Always commits a group, so the group
+// count stays one per tile.
+template <int R, bool kWhole>
+__device__ __forceinline__ void issue_raw(const KernelArgs& a, int32_t index, uint32_t slot_saddr, int q) {
+    using S = RawSlot<R, kWhole>;
+    if (index >= 0 && index < a.num_slots) {
+        const uint8_t* rec = a.cache + static_cast<int64_t>(index) * R;
+#pragma unroll
+        for (int j = q; j < S::kChunks; j += 4) cp_async16(slot_saddr + 16 * j, rec + S::src_offset(j));
+    }
+    cp_async_commit();
+}
+
+// Convert this thread's part of one key from its raw slot into the bf16 tile: the 16-wide NoPE
+// blocks 4c+q (c = 0..7) and, with kRope, RoPE dims [16q, 16q+16). A masked key writes zeros.
+template <int R, bool kRope>
+__device__ __forceinline__ void convert_part(const uint8_t* slot, bool valid, uint8_t* tile, int key, int q) {
+    using S = RawSlot<R, kRope>;
+    if (valid) {
+        uint32_t sw[8];
+        if constexpr (R == 352) {
+            // blocks 4c+q have their scales at bytes 8q + c of the scale field (permuted layout):
+            // one 8-byte load
+            const uint2 s8 = *reinterpret_cast<const uint2*>(slot + S::kScaleOffset + 8 * q);
+#pragma unroll
+            for (int c = 0; c < 8; ++c) sw[c] = ((c < 4 ? s8.x : s8.y) >> (8 * (c & 3))) & 0xFFu;
+        } else {
+            const uint4 s0 = *reinterpret_cast<const uint4*>(slot + S::kScaleOffset);
+            const uint4 s1 = *reinterpret_cast<const uint4*>(slot + S::kScaleOffset + 16);
+            const uint32_t w[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+#pragma unroll
+            for (int c = 0; c < 8; ++c) sw[c] = (w[c] >> (8 * q)) & 0xFFu;   // byte 4c + q
+        }
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            const uint2 codes = *reinterpret_cast<const uint2*>(slot + 32 * c + 8 * q);
+            uint4 lo, hi;
+            dq_block(codes, sw[c], lo, hi);
+            *reinterpret_cast<uint4*>(tile + c * kBlkBytes + swz(key, 2 * q)) = lo;
+            *reinterpret_cast<uint4*>(tile + c * kBlkBytes + swz(key, 2 * q + 1)) = hi;
+        }
+        if constexpr (kRope) {
+            uint4 r0, r1;
+            if constexpr (R == 352) {
+                const uint4 e = *reinterpret_cast<const uint4*>(slot + 256 + 16 * q);
+                r0 = make_uint4(dq_e4m3x2(e.x), dq_e4m3x2(e.x >> 16), dq_e4m3x2(e.y), dq_e4m3x2(e.y >> 16));
+                r1 = make_uint4(dq_e4m3x2(e.z), dq_e4m3x2(e.z >> 16), dq_e4m3x2(e.w), dq_e4m3x2(e.w >> 16));
+            } else {
+                r0 = *reinterpret_cast<const uint4*>(slot + 304 + 32 * q);
+                r1 = *reinterpret_cast<const uint4*>(slot + 304 + 32 * q + 16);
+            }
+            *reinterpret_cast<uint4*>(tile + 8 * kBlkBytes + swz(key, 2 * q)) = r0;
+            *reinterpret_cast<uint4*>(tile + 8 * kBlkBytes + swz(key, 2 * q + 1)) = r1;
+        }
+    } else {
+        const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+        for (int c = 0; c < (kRope ? 9 : 8); ++c) {
+            *reinterpret_cast<uint4*>(tile + c * kBlkBytes + swz(key, 2 * q)) = z;
+            *reinterpret_cast<uint4*>(tile + c * kBlkBytes + swz(key, 2 * q + 1)) = z;
+        }
+    }
+}
+
+// Gather/dequant warps (256 threads, t = 0..255): 4 threads per key, one 64-key tile per
+// iteration. Raw records are copied with cp.async kRawStages tiles ahead into a ring of raw
+// slots; each iteration waits for its own tile's copies, then converts into stage
+// i % kStages of `ring` once the consumer released it (`empty`), and arrives on `full`.
+// With kRope (CTA 0: whole records, RoPE included) the used-key mask of each tile is also
+// published (mask ring + mfull) and K stages are only written once Q has left them (qready).
+template <int R, bool kRope, int kStages, int kStageBytes>
+__device__ __forceinline__ void gather_dequant(const KernelArgs& a, SmemCtl* ctl, uint8_t* ring, uint8_t* raw,
+                                               uint64_t* full, uint64_t* empty, const int32_t* idx_row,
+                                               int key_begin, int key_end, int n_tiles, int t) {
+    using S = RawSlot<R, kRope>;
+    const int key = t >> 2;
+    const int q = t & 3;
+    const int wq = t >> 5;
+    const int lane = t & 31;
+    auto pos_of = [&](int i) { return key_begin + kTile * i + key; };
+    const uint32_t raw_key = smem_addr(raw) + key * S::kKeyBytes;
+    int32_t ix[kRawStages + 1];
+#pragma unroll
+    for (int k = 0; k < kRawStages; ++k) {
+        ix[k] = load_index(idx_row, pos_of(k), key_end);
+        issue_raw<R, kRope>(a, k < n_tiles ? ix[k] : -1, raw_key + k * S::kTileBytes, q);
+    }
+    ix[kRawStages] = load_index(idx_row, pos_of(kRawStages), key_end);
+    for (int i = 0; i < n_tiles; ++i) {
+        const int ks = i % kStages;
+        const int rs = i % kRawStages;
+        const int32_t index = ix[0];
+        if (kRope && q == 0 && index >= a.num_slots && a.status != nullptr) atomicOr(a.status, 0x2u);
+        const bool valid = index >= 0 && index < a.num_slots;
+        cp_async_wait<kRawStages - 1>();      // this thread's copies of tile i have landed
+        __syncwarp();                          // ... and those of the 3 other threads of its key
+        if (i >= kStages && !wait_warp(ctl, &empty[ks], ((i - kStages) / kStages) & 1, a.status)) break;
+        if (kRope && i == 0 && !wait_warp(ctl, &ctl->qready, 0, a.status)) break;   // K stages held Q
+        convert_part<R, kRope>(raw + rs * S::kTileBytes + key * S::kKeyBytes, valid, ring + ks * kStageBytes, key, q);
+        if constexpr (kRope) {
+            const uint32_t used = __ballot_sync(0xffffffffu, valid);
+            if (lane == 0) {
+                uint32_t m = 0;
+#pragma unroll
+                for (int k = 0; k < 8; ++k) m |= ((used >> (4 * k)) & 1u) << k;
+                ctl->mask[i % kMaskSlots][wq] = static_cast<uint8_t>(m);
+                mbar_arrive(&ctl->mfull[i % kMaskSlots]);
+            }
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(&full[ks]);
+        // the raw slot of tile i is free: start tile i + kRawStages there
+        __syncwarp();
+        const int nx = i + kRawStages;
+        issue_raw<R, kRope>(a, nx < n_tiles ? ix[kRawStages] : -1, raw_key + rs * S::kTileBytes, q);
+#pragma unroll
+        for (int k = 0; k < kRawStages; ++k) ix[k] = ix[k + 1];
+        ix[kRawStages] = load_index(idx_row, pos_of(nx + 1), key_end);
+    }
+    cp_async_wait<0>();
+}
+
 template <int R>
-__global__ void __launch_bounds__(kThreads, 1) sparse_decode_kernel(const KernelArgs a) {
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) sparse_decode_kernel(const KernelArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* sQ = smem;
-    uint8_t* sK = smem + kQBytes;
-    SmemCtl* ctl = reinterpret_cast<SmemCtl*>(smem + kQBytes + 2 * kKTileBytes);
+    SmemCtl* ctl = reinterpret_cast<SmemCtl*>(smem);
 
-    const int half = blockIdx.x & 1;                       // which 256 value dims
-    const int split = (blockIdx.x >> 1) % a.splits;
-    const int row = (blockIdx.x >> 1) / a.splits;
+    const int crank = static_cast<int>(cluster_ctarank());   // 0: QK + softmax, 1: PV
+    const int pair = blockIdx.x >> 1;
+    const int split = pair % a.splits;
+    const int row = pair / a.splits;
     const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
     const int key_begin = split * a.keys_per_split;
     const int key_end = min(a.topk, key_begin + a.keys_per_split);
     const int n_tiles = key_end > key_begin ? (key_end - key_begin + kTile - 1) / kTile : 0;
+    const int32_t* idx_row = a.indices + static_cast<int64_t>(row) * a.topk;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(&ctl->kfull[i], 128);
+        for (int i = 0; i < kKStages; ++i) {
+            mbar_init(&ctl->kfull[i], 256);
             mbar_init(&ctl->kempty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
             mbar_init(&ctl->sfull[i], 1);
-            mbar_init(&ctl->pfull[i], 128);
+            mbar_init(&ctl->sfree[i], 128);
+            mbar_init(&ctl->vfull[i], 256);
+            mbar_init(&ctl->vempty[i], 1);
             mbar_init(&ctl->odone[i], 1);
         }
-        mbar_init(&ctl->drain, 1);
+        for (int i = 0; i < kMaskSlots; ++i) mbar_init(&ctl->mfull[i], 8);
+        for (int i = 0; i < kPStages; ++i) {
+            mbar_init(&ctl->pempty[i], 1);
+            mbar_init(&ctl->pfull[i], 4);
+            mbar_init(&ctl->ready[i], 128);
+        }
+        mbar_init(&ctl->qready, 128);
+        mbar_init(&ctl->fin, 4);
+        mbar_init(&ctl->drain, crank == 0 ? 2 : 1);
         ctl->abort = 0u;
         fence_barrier_init();
     }
-    if (warp == 8) {
+    if (warp == 12) {
         tmem_alloc(&ctl->tmem_base, kTmemCols);
         tmem_relinquish();
-    }
-
-    // ---- Q rows -> 128B-swizzled K-major tile (rows >= h_q are zero)
-    {
-        const uint4* qsrc = reinterpret_cast<const uint4*>(a.q + static_cast<int64_t>(row) * a.h_q * kDqk);
-        for (int c = threadIdx.x; c < kHeadsM * (kDqk / 8); c += kThreads) {
-            const int h = c / (kDqk / 8);
-            const int ch = c % (kDqk / 8);
-            uint4 v = make_uint4(0u, 0u, 0u, 0u);
-            if (h < a.h_q) v = __ldg(qsrc + h * (kDqk / 8) + ch);
-            *reinterpret_cast<uint4*>(sQ + (ch >> 3) * kQBlockBytes + swz(h, ch & 7)) = v;
-        }
-        fence_proxy_async_smem();
     }
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = ctl->tmem_base;
+    // Every thread arrives on the cluster barrier now (barriers of both CTAs initialized); only
+    // the threads that touch the peer CTA wait on it before their first remote access, the
+    // others at exit.
+    cluster_arrive();
 
-    if (warp == 8) {
-        // ================= MMA issuer =================
-        const uint32_t idesc_qk = idesc_bf16_f32(kHeadsM, kTile, false, false);
-        const uint32_t idesc_pv = idesc_bf16_f32(kHeadsM, kOCols, false, true);
-        const uint32_t q_base = smem_addr(sQ);
-        const uint32_t k_base = smem_addr(sK);
-        const bool leader = elect_one_in_warp();
-        bool ok = true;
-        auto issue_pv = [&](int j) {
-            const int buf = j & 1;
-            if (!wait_warp(ctl, &ctl->pfull[buf], (j >> 1) & 1, a.status)) return false;
-            tc_fence_after_sync();
-            if (leader) {
-                const uint32_t v_base = k_base + buf * kKTileBytes + (4 * half) * kKBlockBytes;
-#pragma unroll
-                for (int kk = 0; kk < kTile / 16; ++kk) {
-                    const uint64_t bdesc = sdesc_sw128(v_base + kk * 2048, kKBlockBytes, 1024);
-                    mma_ts(tmem, tmem + kSCol + 32 * buf + 8 * kk, bdesc, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
-                }
-                mma_commit(&ctl->kempty[buf]);
-                mma_commit(&ctl->odone[buf]);
+    if (crank == 0) {
+        // Q [128 x 576] bf16 is staged through the two K stages (exactly 144 KB) with coalesced
+        // loads by every thread; row h's 16-byte chunk c sits at h*1152 + (c ^ (h & 7))*16 so the
+        // row reads below are conflict-free. The K stages are written only after qready.
+        uint8_t* sQ = smem + kOffK;
+        {
+            const uint4* src = reinterpret_cast<const uint4*>(a.q + static_cast<int64_t>(row) * a.h_q * kDqk);
+            for (int g = threadIdx.x; g < kHeadsM * (kDqk / 8); g += kThreads) {
+                const int hh = g / (kDqk / 8), c = g % (kDqk / 8);
+                uint4 x = make_uint4(0u, 0u, 0u, 0u);
+                if (hh < a.h_q) x = __ldg(src + g);
+                *reinterpret_cast<uint4*>(sQ + hh * (kDqk * 2) + ((c ^ (hh & 7)) << 4)) = x;
             }
-            __syncwarp();
-            return true;
-        };
-        for (int i = 0; i < n_tiles && ok; ++i) {
-            const int buf = i & 1;
-            ok = wait_warp(ctl, &ctl->kfull[buf], (i >> 1) & 1, a.status);
-            if (!ok) break;
-            tc_fence_after_sync();
-            if (leader) {
-                const uint32_t kb = k_base + buf * kKTileBytes;
-#pragma unroll 4
-                for (int kk = 0; kk < kDqk / 16; ++kk) {
-                    const uint64_t adesc = sdesc_sw128(q_base + (kk >> 2) * kQBlockBytes + (kk & 3) * 32, 16, 1024);
-                    const uint64_t bdesc = sdesc_sw128(kb + (kk >> 2) * kKBlockBytes + (kk & 3) * 32, 16, 1024);
-                    mma_ss(tmem + kSCol + 32 * buf, adesc, bdesc, idesc_qk, kk > 0 ? 1u : 0u);
-                }
-                mma_commit(&ctl->sfull[buf]);
-            }
-            __syncwarp();
-            if (i >= 1) ok = issue_pv(i - 1);
         }
-        if (ok && n_tiles > 0) issue_pv(n_tiles - 1);
-        // drain: every MMA issued by this thread has completed once `drain` flips
-        if (leader) mma_commit(&ctl->drain);
-        __syncwarp();
-        if (!mbar_wait(&ctl->drain, 0)) set_abort(ctl, a.status);
-    } else if (warp >= 4) {
-        // ================= gather / dequant =================
-        const int t = threadIdx.x - 128;
-        const int key = t >> 2;        // 0..31 within the tile
-        const int qd = t & 3;          // owns 16-wide blocks 4c + qd, c = 0..7
-        const int32_t* idx_row = a.indices + static_cast<int64_t>(row) * a.topk;
-        for (int i = 0; i < n_tiles; ++i) {
-            const int buf = i & 1;
-            if (i >= 2 && !wait_or_abort(ctl, &ctl->kempty[buf], ((i - 2) >> 1) & 1, a.status)) break;
-            const int pos = key_begin + i * kTile + key;
-            int64_t slot = pos < key_end ? static_cast<int64_t>(__ldg(idx_row + pos)) : -1;
-            if (slot >= a.num_slots) {
-                if (qd == 0 && a.status != nullptr) atomicOr(a.status, 0x2u);
-                slot = -1;
-            }
-            uint8_t* tile = sK + buf * kKTileBytes;
-            if (slot >= 0) {
-                const uint8_t* rec = a.cache + slot * R;
-                uint32_t sb[8];
-                if constexpr (R == 352) {
-                    const uint2 s8 = __ldg(reinterpret_cast<const uint2*>(rec + 320 + 8 * qd));
+        __syncthreads();
+        if (warp < 4) {
+            // ============ CTA 0, warps 0-3: Q into TMEM, then the softmax ============
+            const int h = threadIdx.x;
+            const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+            {
+                const uint8_t* qrow = sQ + h * (kDqk * 2);
+#pragma unroll 1
+                for (int c = 0; c < 9; ++c) {          // 9 x 64 dims = 9 x 32 columns
+                    uint32_t v[32];
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        sb[c] = (s8.x >> (8 * c)) & 0xFFu;
-                        sb[c + 4] = (s8.y >> (8 * c)) & 0xFFu;
+                    for (int j = 0; j < 8; ++j) {
+                        const uint4 x = *reinterpret_cast<const uint4*>(qrow + (((8 * c + j) ^ (h & 7)) << 4));
+                        v[4 * j] = x.x;
+                        v[4 * j + 1] = x.y;
+                        v[4 * j + 2] = x.z;
+                        v[4 * j + 3] = x.w;
                     }
-                } else {
-                    const uint4 s0 = __ldg(reinterpret_cast<const uint4*>(rec + 256));
-                    const uint4 s1 = __ldg(reinterpret_cast<const uint4*>(rec + 272));
-                    const uint32_t words[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
-#pragma unroll
-                    for (int c = 0; c < 8; ++c) sb[c] = (words[c] >> (8 * qd)) & 0xFFu;   // byte 4c + qd
+                    tmem_st32(lane_base + kColQ + 32 * c, v);
                 }
-#pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    const uint2 codes = __ldg(reinterpret_cast<const uint2*>(rec + 32 * c + 8 * qd));
-                    uint4 lo, hi;
-                    dq_block(codes, sb[c], lo, hi);
-                    uint8_t* blk = tile + c * kKBlockBytes;
-                    *reinterpret_cast<uint4*>(blk + swz(key, 2 * qd)) = lo;
-                    *reinterpret_cast<uint4*>(blk + swz(key, 2 * qd + 1)) = hi;
-                }
-                uint4 r0, r1;
-                if constexpr (R == 352) {
-                    const uint4 e = __ldg(reinterpret_cast<const uint4*>(rec + 256 + 16 * qd));
-                    r0 = make_uint4(dq_e4m3x2(e.x), dq_e4m3x2(e.x >> 16), dq_e4m3x2(e.y), dq_e4m3x2(e.y >> 16));
-                    r1 = make_uint4(dq_e4m3x2(e.z), dq_e4m3x2(e.z >> 16), dq_e4m3x2(e.w), dq_e4m3x2(e.w >> 16));
-                } else {
-                    r0 = __ldg(reinterpret_cast<const uint4*>(rec + 304 + 32 * qd));
-                    r1 = __ldg(reinterpret_cast<const uint4*>(rec + 304 + 32 * qd + 16));
-                }
-                uint8_t* blk = tile + 8 * kKBlockBytes;
-                *reinterpret_cast<uint4*>(blk + swz(key, 2 * qd)) = r0;
-                *reinterpret_cast<uint4*>(blk + swz(key, 2 * qd + 1)) = r1;
-            } else {
-                const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-                for (int c = 0; c < kDBlocks; ++c) {
-                    uint8_t* blk = tile + c * kKBlockBytes;
-                    *reinterpret_cast<uint4*>(blk + swz(key, 2 * qd)) = z;
-                    *reinterpret_cast<uint4*>(blk + swz(key, 2 * qd + 1)) = z;
-                }
+                tmem_wait_st();
+                tc_fence_before_sync();
+                mbar_arrive(&ctl->qready);
             }
-            fence_proxy_async_smem();
-            mbar_arrive(&ctl->kfull[buf]);
-        }
-    } else {
-        // ================= softmax / epilogue (thread = head row) =================
-        const int h = threadIdx.x;                              // TMEM lane
-        const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-        const int32_t* idx_row = a.indices + static_cast<int64_t>(row) * a.topk;
-        float m_ref = -INFINITY;   // reference max, log2 units of scaled logits
-        float l = 0.0f;            // sum of 2^(s - m_ref) over used keys
-        bool ok = true;
-        int done_tiles = 0;
-        for (int i = 0; i < n_tiles; ++i) {
-            const int buf = i & 1;
-            // used-key mask of this tile
-            uint32_t used = 0u;
-            const int pos0 = key_begin + i * kTile;
-#pragma unroll 4
-            for (int j = 0; j < kTile; ++j) {
-                if (pos0 + j < key_end) {
-                    const int32_t s = __ldg(idx_row + pos0 + j);
-                    if (s >= 0 && s < a.num_slots) used |= 1u << j;
-                }
-            }
-            ok = wait_warp(ctl, &ctl->sfull[buf], (i >> 1) & 1, a.status);
-            if (!ok) break;
-            tc_fence_after_sync();
-            uint32_t sr[32];
-            tmem_ld32(lane_base + kSCol + 32 * buf, sr);
-            tmem_wait_ld();
-            float s[32];
-            float tile_max = -INFINITY;
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                s[j] = ((used >> j) & 1u) ? __uint_as_float(sr[j]) * a.scale_log2 : -INFINITY;
-                tile_max = fmaxf(tile_max, s[j]);
-            }
-            bool rescale = false;
-            float alpha = 1.0f;
-            if (tile_max > m_ref + kRescaleThreshold) {
-                if (m_ref != -INFINITY) {
-                    alpha = exp2f(m_ref - tile_max);
-                    rescale = true;
-                }
-                m_ref = tile_max;
-            }
-            l *= alpha;
-            uint32_t p[16];
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const float p0 = (m_ref == -INFINITY) ? 0.0f : exp2f(s[2 * j] - m_ref);
-                const float p1 = (m_ref == -INFINITY) ? 0.0f : exp2f(s[2 * j + 1] - m_ref);
-                l += p0 + p1;
-                p[j] = pack_bf16x2(p0, p1);
-            }
-            if (__any_sync(0xffffffffu, rescale) && i > 0) {
-                ok = wait_warp(ctl, &ctl->odone[(i - 1) & 1], ((i - 1) >> 1) & 1, a.status);
+            cluster_wait();
+            // row h of CTA 1's P slot 0 (128B-swizzled K-major rows; chunk c at (c ^ (h & 7)) * 16)
+            const uint32_t peer_p = mapa_shared(smem_addr(smem + kOffP) + (h >> 3) * 1024 + (h & 7) * 128, 1);
+            const uint32_t peer_alpha = mapa_shared(smem_addr(smem + kOffAlpha) + 4 * h, 1);
+            const uint32_t peer_fin = mapa_shared(smem_addr(smem + kOffFin) + 8 * h, 1);
+            const uint32_t peer_pfull0 = mapa_shared(smem_addr(&ctl->pfull[0]), 1);
+            const uint32_t peer_finbar = mapa_shared(smem_addr(&ctl->fin), 1);
+            float m_ref = -INFINITY;   // reference max, log2 units of scaled logits
+            float l = 0.0f;            // sum of 2^(s - m_ref) over used keys
+            bool ok = true;
+            for (int i = 0; i < n_tiles && ok; ++i) {
+                const int b = i & 1;
+                ok = wait_warp(ctl, &ctl->sfull[b], (i >> 1) & 1, a.status);
                 if (!ok) break;
                 tc_fence_after_sync();
-#pragma unroll 1
-                for (int c = 0; c < kOCols / 32; ++c) {
-                    uint32_t o[32];
-                    tmem_ld32(lane_base + 32 * c, o);
-                    tmem_wait_ld();
+                uint32_t s[64];
+                tmem_ld32(lane_base + kColS + 64 * b, *reinterpret_cast<uint32_t(*)[32]>(s));
+                tmem_ld32(lane_base + kColS + 64 * b + 32, *reinterpret_cast<uint32_t(*)[32]>(s + 32));
+                tmem_wait_ld();
+                tc_fence_before_sync();
+                mbar_arrive(&ctl->sfree[b]);
+                ok = wait_warp(ctl, &ctl->mfull[i % kMaskSlots], (i / kMaskSlots) & 1, a.status);
+                if (!ok) break;
+                const uint64_t used = *reinterpret_cast<const volatile uint64_t*>(ctl->mask[i % kMaskSlots]);
+                // ---- online softmax (log2 domain, lazy reference max)
+                float mx0 = -INFINITY, mx1 = -INFINITY;
+                if (used == ~0ull) {          // every key of the tile used (the common case)
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
-                    tmem_st32(lane_base + 32 * c, o);
-                }
-            }
-            tmem_st16(lane_base + kSCol + 32 * buf, p);
-            tmem_wait_st();
-            tc_fence_before_sync();
-            mbar_arrive(&ctl->pfull[buf]);
-            done_tiles = i + 1;
-        }
-        // ---- epilogue
-        bool have_o = false;
-        if (ok && done_tiles == n_tiles && n_tiles > 0) {
-            have_o = wait_warp(ctl, &ctl->odone[(n_tiles - 1) & 1], ((n_tiles - 1) >> 1) & 1, a.status);
-            if (have_o) tc_fence_after_sync();
-        }
-        const bool empty = !(l > 0.0f);
-        const bool write = h < a.h_q;
-        float inv = 0.0f;
-        float lse_nat = -INFINITY;
-        if (!empty) {
-            lse_nat = (m_ref + log2f(l)) * kLn2;
-            float denom = l;
-            if (a.splits == 1 && a.sink != nullptr) denom += exp2f(__ldg(a.sink + (h < a.h_q ? h : 0)) * kLog2e - m_ref);
-            inv = 1.0f / denom;
-        }
-        const int64_t rh = static_cast<int64_t>(row) * a.h_q + h;
-        if (a.splits == 1) {
-            __nv_bfloat16* dst = a.out + rh * 512 + 256 * half;
-#pragma unroll 1
-            for (int c = 0; c < kOCols / 32; ++c) {
-                uint32_t o[32];
-                if (have_o) {
-                    tmem_ld32(lane_base + 32 * c, o);
-                    tmem_wait_ld();
-                }
-                if (write) {
+                    for (int j = 0; j < 64; j += 2) {
+                        const float v0 = __uint_as_float(s[j]) * a.scale_log2;
+                        const float v1 = __uint_as_float(s[j + 1]) * a.scale_log2;
+                        s[j] = __float_as_uint(v0);
+                        s[j + 1] = __float_as_uint(v1);
+                        mx0 = fmaxf(mx0, v0);
+                        mx1 = fmaxf(mx1, v1);
+                    }
+                } else {
 #pragma unroll
-                    for (int v = 0; v < 4; ++v) {
-                        uint4 w;
-                        uint32_t* wp = reinterpret_cast<uint32_t*>(&w);
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float x0 = (have_o && !empty) ? __uint_as_float(o[8 * v + 2 * e]) * inv : 0.0f;
-                            const float x1 = (have_o && !empty) ? __uint_as_float(o[8 * v + 2 * e + 1]) * inv : 0.0f;
-                            wp[e] = pack_bf16x2(x0, x1);
-                        }
-                        *reinterpret_cast<uint4*>(dst + 32 * c + 8 * v) = w;
+                    for (int j = 0; j < 64; j += 2) {
+                        const float v0 = ((used >> j) & 1ull) ? __uint_as_float(s[j]) * a.scale_log2 : -INFINITY;
+                        const float v1 =
+                            ((used >> (j + 1)) & 1ull) ? __uint_as_float(s[j + 1]) * a.scale_log2 : -INFINITY;
+                        s[j] = __float_as_uint(v0);
+                        s[j + 1] = __float_as_uint(v1);
+                        mx0 = fmaxf(mx0, v0);
+                        mx1 = fmaxf(mx1, v1);
                     }
                 }
+                const float tile_max = fmaxf(mx0, mx1);
+                float alpha = 1.0f;
+                if (tile_max > m_ref + kRescaleThreshold) {
+                    if (m_ref != -INFINITY) alpha = ex2_approx(m_ref - tile_max);
+                    m_ref = tile_max;
+                }
+                uint32_t p[32];
+                if (m_ref != -INFINITY) {
+                    float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
+#pragma unroll
+                    for (int j = 0; j < 32; j += 2) {
+                        const float p0 = ex2_approx(__uint_as_float(s[2 * j]) - m_ref);
+                        const float p1 = ex2_approx(__uint_as_float(s[2 * j + 1]) - m_ref);
+                        const float p2 = ex2_approx(__uint_as_float(s[2 * j + 2]) - m_ref);
+                        const float p3 = ex2_approx(__uint_as_float(s[2 * j + 3]) - m_ref);
+                        l0 += p0;
+                        l1 += p1;
+                        l2 += p2;
+                        l3 += p3;
+                        p[j] = pack_bf16x2(p0, p1);
+                        p[j + 1] = pack_bf16x2(p2, p3);
+                    }
+                    l = l * alpha + ((l0 + l1) + (l2 + l3));
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) p[j] = 0u;
+                }
+                // ---- P row h and alpha -> CTA 1's slot (i % kPStages), once its PV released it
+                const int ps = i % kPStages;
+                if (i >= kPStages) {
+                    ok = wait_warp(ctl, &ctl->pempty[ps], ((i / kPStages) - 1) & 1, a.status);
+                    if (!ok) break;
+                }
+                const uint32_t dst = peer_p + ps * kPBytes;
+                const uint32_t bar = peer_pfull0 + 8 * ps;
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    st_async_u4(dst + ((c ^ (h & 7)) << 4),
+                                make_uint4(p[4 * c], p[4 * c + 1], p[4 * c + 2], p[4 * c + 3]), bar);
+                st_async_f32(peer_alpha + ps * kHeadsM * 4, alpha, bar);
             }
-            if (write && half == 0) a.lse[rh] = lse_nat;
+            // ---- epilogue: running max and sum to CTA 1; lse here
+            if (ok) {
+                st_async_v2(peer_fin, m_ref, l, peer_finbar);
+            }
+            const bool write = h < a.h_q;
+            float lse_nat = -INFINITY;
+            if (l > 0.0f) lse_nat = (m_ref + log2f(l)) * kLn2;
+            if (write) {
+                if (a.splits == 1) {
+                    a.lse[static_cast<int64_t>(row) * a.h_q + h] = lse_nat;
+                } else {
+                    a.part_lse[(static_cast<int64_t>(row) * a.splits + split) * a.h_q + h] = lse_nat;
+                }
+            }
+        } else if (warp < 12) {
+            // ============ CTA 0, warps 4-11: gather/dequant of whole records ============
+            gather_dequant<R, true, kKStages, kKTileBytes>(a, ctl, smem + kOffK, smem + kOffRaw0, ctl->kfull,
+                                                           ctl->kempty, idx_row, key_begin, key_end, n_tiles,
+                                                           threadIdx.x - 128);
         } else {
-            const int64_t ph = (static_cast<int64_t>(row) * a.splits + split) * a.h_q + h;
-            float* dst = a.part_out + ph * 512 + 256 * half;
-#pragma unroll 1
-            for (int c = 0; c < kOCols / 32; ++c) {
-                uint32_t o[32];
-                if (have_o) {
-                    tmem_ld32(lane_base + 32 * c, o);
-                    tmem_wait_ld();
-                }
-                if (write) {
+            // ============ CTA 0, warps 12-13: QK issuers (warp 12 even tiles, warp 13 odd tiles) ============
+            const uint32_t idesc_qk = idesc_bf16_f32(kHeadsM, kTile, false, false);
+            const uint64_t kdesc0 = sdesc_sw128(smem_addr(smem + kOffK), 16, 1024);
+            const bool leader = elect_one_in_warp();
+            bool ok = wait_warp(ctl, &ctl->qready, 0, a.status);
+            for (int i = warp - 12; i < n_tiles && ok; i += 2) {
+                const int ks = i % kKStages;
+                const int b = i & 1;
+                ok = wait_warp(ctl, &ctl->kfull[ks], (i / kKStages) & 1, a.status);
+                if (ok && i >= 2) ok = wait_warp(ctl, &ctl->sfree[b], ((i - 2) >> 1) & 1, a.status);
+                if (!ok) break;
+                tc_fence_after_sync();
+                if (leader) {
+                    const uint64_t kd = kdesc0 + static_cast<uint64_t>((ks * kKTileBytes) >> 4);
+                    const uint32_t d = tmem + kColS + 64 * b;
 #pragma unroll
-                    for (int v = 0; v < 8; ++v) {
-                        float4 w;
-                        w.x = (have_o && !empty) ? __uint_as_float(o[4 * v + 0]) * inv : 0.0f;
-                        w.y = (have_o && !empty) ? __uint_as_float(o[4 * v + 1]) * inv : 0.0f;
-                        w.z = (have_o && !empty) ? __uint_as_float(o[4 * v + 2]) * inv : 0.0f;
-                        w.w = (have_o && !empty) ? __uint_as_float(o[4 * v + 3]) * inv : 0.0f;
-                        *reinterpret_cast<float4*>(dst + 32 * c + 4 * v) = w;
+                    for (int kk = 0; kk < 36; ++kk)
+                        mma_ts(d, tmem + kColQ + 8 * kk, kd + (((kk >> 2) * kBlkBytes + (kk & 3) * 32) >> 4), idesc_qk,
+                               kk > 0 ? 1u : 0u);
+                    mma_commit(&ctl->kempty[ks]);
+                    mma_commit(&ctl->sfull[b]);
+                }
+                __syncwarp();
+            }
+            if (leader) mma_commit(&ctl->drain);
+            __syncwarp();
+            if (!mbar_wait(&ctl->drain, 0)) set_abort(ctl, a.status);
+        }
+    } else {
+        if (warp < 4) {
+            // ============ CTA 1, warps 0-3: per-tile alpha check / O rescale, then the output ============
+            const int h = threadIdx.x;
+            const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+            const float* s_alpha = reinterpret_cast<const float*>(smem + kOffAlpha);
+            bool ok = true;
+            for (int i = 0; i < n_tiles && ok; ++i) {
+                const int ps = i % kPStages;
+                if (lane == 0) mbar_arrive_expect_tx(&ctl->pfull[ps], 32 * (128 + 4));
+                ok = wait_warp(ctl, &ctl->pfull[ps], (i / kPStages) & 1, a.status);
+                if (!ok) break;
+                const float alpha = s_alpha[ps * kHeadsM + h];
+                if (__any_sync(0xffffffffu, alpha != 1.0f) && i > 0) {
+                    ok = wait_warp(ctl, &ctl->odone[(i - 1) & 1], ((i - 1) >> 1) & 1, a.status);
+                    if (!ok) break;
+                    tc_fence_after_sync();
+#pragma unroll 1
+                    for (int c = 0; c < 16; ++c) {
+                        uint32_t o[32];
+                        tmem_ld32(lane_base + kColO + 32 * c, o);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
+                        tmem_st32(lane_base + kColO + 32 * c, o);
+                    }
+                    tmem_wait_st();
+                }
+                fence_proxy_async_smem();     // P written by the peer's st.async, read by the MMA
+                tc_fence_before_sync();
+                mbar_arrive(&ctl->ready[ps]);
+            }
+            // ---- output: O / (l + sink term) for this CTA's row h
+            if (lane == 0) mbar_arrive_expect_tx(&ctl->fin, 32 * 8);
+            bool have_fin = ok && wait_warp(ctl, &ctl->fin, 0, a.status);
+            bool have_o = false;
+            if (have_fin && n_tiles > 0) {
+                have_o = wait_warp(ctl, &ctl->odone[(n_tiles - 1) & 1], ((n_tiles - 1) >> 1) & 1, a.status);
+                if (have_o) tc_fence_after_sync();
+            }
+            float m_ref = -INFINITY, l = 0.0f;
+            if (have_fin) {
+                const float2 f = *reinterpret_cast<const float2*>(smem + kOffFin + 8 * h);
+                m_ref = f.x;
+                l = f.y;
+            }
+            const bool empty = !(l > 0.0f);
+            const bool write = h < a.h_q;
+            float inv = 0.0f;
+            if (!empty) {
+                float denom = l;
+                if (a.splits == 1 && a.sink != nullptr)
+                    denom += exp2f(__ldg(a.sink + (h < a.h_q ? h : 0)) * kLog2e - m_ref);
+                inv = 1.0f / denom;
+            }
+            const bool use_o = have_o && !empty;
+            const int64_t rh = static_cast<int64_t>(row) * a.h_q + h;
+            if (a.splits == 1) {
+                __nv_bfloat16* dst = a.out + rh * 512;
+#pragma unroll 1
+                for (int c = 0; c < 16; ++c) {
+                    uint32_t o[32];
+                    if (have_o) {
+                        tmem_ld32(lane_base + kColO + 32 * c, o);
+                        tmem_wait_ld();
+                    }
+                    if (write) {
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            uint4 w;
+                            uint32_t* wp = reinterpret_cast<uint32_t*>(&w);
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const float x0 = use_o ? __uint_as_float(o[8 * v + 2 * e]) * inv : 0.0f;
+                                const float x1 = use_o ? __uint_as_float(o[8 * v + 2 * e + 1]) * inv : 0.0f;
+                                wp[e] = pack_bf16x2(x0, x1);
+                            }
+                            *reinterpret_cast<uint4*>(dst + 32 * c + 8 * v) = w;
+                        }
+                    }
+                }
+            } else {
+                const int64_t ph = (static_cast<int64_t>(row) * a.splits + split) * a.h_q + h;
+                float* dst = a.part_out + ph * 512;
+#pragma unroll 1
+                for (int c = 0; c < 16; ++c) {
+                    uint32_t o[32];
+                    if (have_o) {
+                        tmem_ld32(lane_base + kColO + 32 * c, o);
+                        tmem_wait_ld();
+                    }
+                    if (write) {
+#pragma unroll
+                        for (int v = 0; v < 8; ++v) {
+                            float4 w;
+                            w.x = use_o ? __uint_as_float(o[4 * v + 0]) * inv : 0.0f;
+                            w.y = use_o ? __uint_as_float(o[4 * v + 1]) * inv : 0.0f;
+                            w.z = use_o ? __uint_as_float(o[4 * v + 2]) * inv : 0.0f;
+                            w.w = use_o ? __uint_as_float(o[4 * v + 3]) * inv : 0.0f;
+                            *reinterpret_cast<float4*>(dst + 32 * c + 4 * v) = w;
+                        }
                     }
                 }
             }
-            if (write && half == 0) a.part_lse[ph] = lse_nat;
+        } else if (warp < 12) {
+            // ============ CTA 1, warps 4-11: gather/dequant of the NoPE halves (V) ============
+            gather_dequant<R, false, kVStages, kVTileBytes>(a, ctl, smem + kOffV, smem + kOffRaw1, ctl->vfull,
+                                                            ctl->vempty, idx_row, key_begin, key_end, n_tiles,
+                                                            threadIdx.x - 128);
+        } else if (warp == 12) {
+            // ============ CTA 1, warp 12: PV issuer (warp 13 idle) ============
+            cluster_wait();          // CTA 0's pempty barriers exist before the first multicast commit
+            const uint32_t idesc_pv = idesc_bf16_f32(kHeadsM, 256, false, true);
+            const uint64_t pdesc0 = sdesc_sw128(smem_addr(smem + kOffP), 16, 1024);
+            const uint64_t vdesc0 = sdesc_sw128(smem_addr(smem + kOffV), kBlkBytes, 1024);
+            const bool leader = elect_one_in_warp();
+            bool ok = true;
+            for (int i = 0; i < n_tiles && ok; ++i) {
+                const int vs = i % kVStages;
+                const int ps = i % kPStages;
+                ok = wait_warp(ctl, &ctl->vfull[vs], (i / kVStages) & 1, a.status);
+                if (ok) ok = wait_warp(ctl, &ctl->ready[ps], (i / kPStages) & 1, a.status);
+                if (!ok) break;
+                tc_fence_after_sync();
+                if (leader) {
+                    const uint64_t pd = pdesc0 + static_cast<uint64_t>((ps * kPBytes) >> 4);
+                    const uint64_t vd = vdesc0 + static_cast<uint64_t>((vs * kVTileBytes) >> 4);
+#pragma unroll
+                    for (int half = 0; half < 2; ++half)
+#pragma unroll
+                        for (int kk = 0; kk < kTile / 16; ++kk)
+                            mma_ss(tmem + kColO + 256 * half, pd + ((kk * 32) >> 4),
+                                   vd + ((half * 4 * kBlkBytes + kk * 2048) >> 4), idesc_pv, (i > 0 || kk > 0) ? 1u : 0u);
+                    mma_commit(&ctl->vempty[vs]);
+                    mma_commit(&ctl->odone[i & 1]);
+                    mma_commit_multicast(&ctl->pempty[ps], 0x1);
+                }
+                __syncwarp();
+            }
+            if (leader) mma_commit(&ctl->drain);
+            __syncwarp();
+            if (!mbar_wait(&ctl->drain, 0)) set_abort(ctl, a.status);
         }
     }
 
+    // threads that have not waited on the prologue's cluster phase do so now
+    const bool waited = (crank == 0 && warp < 4) || (crank == 1 && warp == 12);
+    if (!waited) cluster_wait();
     tc_fence_before_sync();
-    __syncthreads();
-    if (warp == 8) {
+    cluster_sync();          // no CTA leaves while its peer may still touch its shared memory
+    if (warp == 12) {
         tc_fence_after_sync();
         tmem_dealloc(tmem, kTmemCols);
     }
