@@ -85,10 +85,11 @@ NVFP4_MLA_API int nvfp4_mla_quantize_append(const void* kv_latent, int64_t laten
 /*
  * Scratch size of nvfp4_sparse_mla_decode for a problem (host-only, no CUDA call).
  *   num_splits: the top-k list of each query row is cut into num_splits consecutive parts
- *   computed in parallel and merged by a second kernel; 0 lets the library choose from the
- *   problem size and the SM count of the current device (then this call reads the device
- *   attribute). The workspace holds fp32 partial outputs and log-sum-exps of every part;
- *   it is 0 bytes when a single part is used.
+ *   computed in parallel and merged by a second kernel (launched as a programmatic dependent
+ *   of the first on the same stream); 0 lets the library choose from the problem size and the
+ *   SM count of the current device (then this call reads the device attribute). The workspace
+ *   holds fp32 partial outputs and log-sum-exps of every part; it is 0 bytes when a single
+ *   part is used.
  * Returns NVFP4_MLA_OK and sets *bytes, or an error code for an invalid problem.
  */
 NVFP4_MLA_API int nvfp4_sparse_mla_decode_workspace_size(int32_t batch, int32_t s_q, int32_t h_q,
@@ -114,7 +115,8 @@ NVFP4_MLA_API int nvfp4_sparse_mla_decode_workspace_size(int32_t batch, int32_t 
  *                entries (sink excluded). A row with no used entry gets out = 0, lse = -inf.
  *   num_splits   0 = library choice, else 1..64 (see ..._workspace_size).
  *   workspace    device scratch of at least the size ..._workspace_size reports for the same
- *                arguments, 256-byte aligned; may be NULL when that size is 0.
+ *                arguments, 256-byte aligned; may be NULL when that size is 0. Its contents
+ *                need no initialization.
  *   dev_status   nullable device uint32 (see NVFP4_MLA_DEV_*).
  * Precision: dequantized keys are exact in bf16; the two contractions run on tcgen05 bf16
  * MMAs with fp32 accumulation; softmax in fp32; `out` is rounded to bf16 once.

@@ -28,7 +28,7 @@ struct DecodeArgs {
     float* lse;                // [rows, h_q]
     int splits;
     float* part_out;           // fp32 [rows, splits, h_q, 512] when splits > 1
-    float* part_lse;           // fp32 [rows, splits, h_q]
+    float* part_lse;           // fp32 [rows, splits, h_q], log2 domain
     uint32_t* dev_status;
 };
 

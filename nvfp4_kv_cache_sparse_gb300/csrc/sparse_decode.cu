@@ -340,6 +340,60 @@ __device__ __forceinline__ void gather_dequant(const KernelArgs& a, SmemCtl* ctl
     cp_async_wait<0>();
 }
 
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t threads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// CTA 1, warps 0-3 (thread h = TMEM lane h): O * factor for the row's 128 x 512 block, written
+// out (bf16 `out` when there is one split, fp32 partial otherwise) through shared memory so
+// that every warp store covers whole 128-byte lines. Four quarters of 128 columns, staged in
+// the two V stages alternately (row h at h * 512, 16-byte chunk k at slot k ^ (h & 7)).
+__device__ __forceinline__ void write_rows(const KernelArgs& a, uint8_t* smem, uint32_t lane_base, bool use_o,
+                                           float factor, int row, int split, int warp, int lane, int h) {
+#pragma unroll 1
+    for (int qt = 0; qt < 4; ++qt) {
+        uint8_t* buf = smem + kOffV + (qt & 1) * kVTileBytes;
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+            uint32_t o[32];
+            if (use_o) {
+                tmem_ld32(lane_base + kColO + 128 * qt + 32 * c, o);
+                tmem_wait_ld();
+            }
+#pragma unroll
+            for (int v = 0; v < 8; ++v) {
+                float4 w;
+                w.x = use_o ? __uint_as_float(o[4 * v + 0]) * factor : 0.0f;
+                w.y = use_o ? __uint_as_float(o[4 * v + 1]) * factor : 0.0f;
+                w.z = use_o ? __uint_as_float(o[4 * v + 2]) * factor : 0.0f;
+                w.w = use_o ? __uint_as_float(o[4 * v + 3]) * factor : 0.0f;
+                *reinterpret_cast<float4*>(buf + h * 512 + (((8 * c + v) ^ (h & 7)) << 4)) = w;
+            }
+        }
+        named_bar_sync(1, 128);
+        const int nrows = min(32, a.h_q - 32 * warp);
+        if (a.splits == 1) {
+            __nv_bfloat16* dst = a.out + (static_cast<int64_t>(row) * a.h_q + 32 * warp) * 512 + 128 * qt + 4 * lane;
+#pragma unroll 4
+            for (int r = 0; r < nrows; ++r) {
+                const int hh = 32 * warp + r;
+                const float4 x = *reinterpret_cast<const float4*>(buf + hh * 512 + ((lane ^ (hh & 7)) << 4));
+                *reinterpret_cast<uint2*>(dst + static_cast<int64_t>(r) * 512) =
+                    make_uint2(pack_bf16x2(x.x, x.y), pack_bf16x2(x.z, x.w));
+            }
+        } else {
+            float* dst = a.part_out + ((static_cast<int64_t>(row) * a.splits + split) * a.h_q + 32 * warp) * 512 +
+                         128 * qt + 4 * lane;
+#pragma unroll 4
+            for (int r = 0; r < nrows; ++r) {
+                const int hh = 32 * warp + r;
+                *reinterpret_cast<float4*>(dst + static_cast<int64_t>(r) * 512) =
+                    *reinterpret_cast<const float4*>(buf + hh * 512 + ((lane ^ (hh & 7)) << 4));
+            }
+        }
+    }
+}
+
 template <int R>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) sparse_decode_kernel(const KernelArgs a) {
     extern __shared__ uint8_t smem_raw[];
@@ -389,6 +443,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) sparse_
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = ctl->tmem_base;
+    asm volatile("griddepcontrol.launch_dependents;");   // the split merge may be scheduled now
     // Every thread arrives on the cluster barrier now (barriers of both CTAs initialized); only
     // the threads that touch the peer CTA wait on it before their first remote access, the
     // others at exit.
@@ -456,31 +511,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) sparse_
                 ok = wait_warp(ctl, &ctl->mfull[i % kMaskSlots], (i / kMaskSlots) & 1, a.status);
                 if (!ok) break;
                 const uint64_t used = *reinterpret_cast<const volatile uint64_t*>(ctl->mask[i % kMaskSlots]);
-                // ---- online softmax (log2 domain, lazy reference max)
-                float mx0 = -INFINITY, mx1 = -INFINITY;
-                if (used == ~0ull) {          // every key of the tile used (the common case)
+                // ---- online softmax (log2 domain, lazy reference max): z = s * scale_log2.
+                // Common case (every key used, scale > 0): the max is taken on the raw scores and
+                // each z - m is one fused multiply-add; otherwise masked keys become -inf first.
+                float zs = a.scale_log2;      // multiplier applied to s[] below
+                float tile_max;
+                if (used == ~0ull && zs > 0.0f) {
+                    float m0 = -INFINITY, m1 = -INFINITY;
 #pragma unroll
-                    for (int j = 0; j < 64; j += 2) {
-                        const float v0 = __uint_as_float(s[j]) * a.scale_log2;
-                        const float v1 = __uint_as_float(s[j + 1]) * a.scale_log2;
-                        s[j] = __float_as_uint(v0);
-                        s[j + 1] = __float_as_uint(v1);
-                        mx0 = fmaxf(mx0, v0);
-                        mx1 = fmaxf(mx1, v1);
+                    for (int j = 0; j < 64; j += 4) {
+                        m0 = fmax3(m0, __uint_as_float(s[j]), __uint_as_float(s[j + 1]));
+                        m1 = fmax3(m1, __uint_as_float(s[j + 2]), __uint_as_float(s[j + 3]));
                     }
+                    tile_max = fmaxf(m0, m1) * zs;
                 } else {
+                    float m0 = -INFINITY, m1 = -INFINITY;
 #pragma unroll
                     for (int j = 0; j < 64; j += 2) {
-                        const float v0 = ((used >> j) & 1ull) ? __uint_as_float(s[j]) * a.scale_log2 : -INFINITY;
-                        const float v1 =
-                            ((used >> (j + 1)) & 1ull) ? __uint_as_float(s[j + 1]) * a.scale_log2 : -INFINITY;
+                        const float v0 = ((used >> j) & 1ull) ? __uint_as_float(s[j]) * zs : -INFINITY;
+                        const float v1 = ((used >> (j + 1)) & 1ull) ? __uint_as_float(s[j + 1]) * zs : -INFINITY;
                         s[j] = __float_as_uint(v0);
                         s[j + 1] = __float_as_uint(v1);
-                        mx0 = fmaxf(mx0, v0);
-                        mx1 = fmaxf(mx1, v1);
+                        m0 = fmaxf(m0, v0);
+                        m1 = fmaxf(m1, v1);
                     }
+                    tile_max = fmaxf(m0, m1);
+                    zs = 1.0f;
                 }
-                const float tile_max = fmaxf(mx0, mx1);
                 float alpha = 1.0f;
                 if (tile_max > m_ref + kRescaleThreshold) {
                     if (m_ref != -INFINITY) alpha = ex2_approx(m_ref - tile_max);
@@ -488,21 +545,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) sparse_
                 }
                 uint32_t p[32];
                 if (m_ref != -INFINITY) {
-                    float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
+                    const uint64_t mul2 = f32x2_pack(zs, zs);
+                    const uint64_t neg_m2 = f32x2_pack(-m_ref, -m_ref);
+                    uint64_t la = f32x2_pack(0.0f, 0.0f), lb = la;
 #pragma unroll
-                    for (int j = 0; j < 32; j += 2) {
-                        const float p0 = ex2_approx(__uint_as_float(s[2 * j]) - m_ref);
-                        const float p1 = ex2_approx(__uint_as_float(s[2 * j + 1]) - m_ref);
-                        const float p2 = ex2_approx(__uint_as_float(s[2 * j + 2]) - m_ref);
-                        const float p3 = ex2_approx(__uint_as_float(s[2 * j + 3]) - m_ref);
-                        l0 += p0;
-                        l1 += p1;
-                        l2 += p2;
-                        l3 += p3;
-                        p[j] = pack_bf16x2(p0, p1);
-                        p[j + 1] = pack_bf16x2(p2, p3);
+                    for (int j = 0; j < 64; j += 4) {
+                        const float2 z0 = f32x2_unpack(
+                            f32x2_fma(f32x2_pack(__uint_as_float(s[j]), __uint_as_float(s[j + 1])), mul2, neg_m2));
+                        const float2 z1 = f32x2_unpack(
+                            f32x2_fma(f32x2_pack(__uint_as_float(s[j + 2]), __uint_as_float(s[j + 3])), mul2, neg_m2));
+                        const float p0 = ex2_approx(z0.x), p1 = ex2_approx(z0.y);
+                        const float p2 = ex2_approx(z1.x), p3 = ex2_approx(z1.y);
+                        la = f32x2_add(la, f32x2_pack(p0, p1));
+                        lb = f32x2_add(lb, f32x2_pack(p2, p3));
+                        p[j / 2] = pack_bf16x2(p0, p1);
+                        p[j / 2 + 1] = pack_bf16x2(p2, p3);
                     }
-                    l = l * alpha + ((l0 + l1) + (l2 + l3));
+                    const float2 sa = f32x2_unpack(la), sb = f32x2_unpack(lb);
+                    l = l * alpha + ((sa.x + sa.y) + (sb.x + sb.y));
                 } else {
 #pragma unroll
                     for (int j = 0; j < 32; ++j) p[j] = 0u;
@@ -521,20 +581,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) sparse_
                                 make_uint4(p[4 * c], p[4 * c + 1], p[4 * c + 2], p[4 * c + 3]), bar);
                 st_async_f32(peer_alpha + ps * kHeadsM * 4, alpha, bar);
             }
-            // ---- epilogue: running max and sum to CTA 1; lse here
-            if (ok) {
-                st_async_v2(peer_fin, m_ref, l, peer_finbar);
-            }
-            const bool write = h < a.h_q;
-            float lse_nat = -INFINITY;
-            if (l > 0.0f) lse_nat = (m_ref + log2f(l)) * kLn2;
-            if (write) {
-                if (a.splits == 1) {
-                    a.lse[static_cast<int64_t>(row) * a.h_q + h] = lse_nat;
-                } else {
-                    a.part_lse[(static_cast<int64_t>(row) * a.splits + split) * a.h_q + h] = lse_nat;
-                }
-            }
+            // ---- running max and sum to CTA 1, which writes out and lse
+            if (ok) st_async_v2(peer_fin, m_ref, l, peer_finbar);
         } else if (warp < 12) {
             // ============ CTA 0, warps 4-11: gather/dequant of whole records ============
             gather_dequant<R, true, kKStages, kKTileBytes>(a, ctl, smem + kOffK, smem + kOffRaw0, ctl->kfull,
@@ -601,9 +649,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) sparse_
                 tc_fence_before_sync();
                 mbar_arrive(&ctl->ready[ps]);
             }
-            // ---- output: O / (l + sink term) for this CTA's row h
+            // ---- output
             if (lane == 0) mbar_arrive_expect_tx(&ctl->fin, 32 * 8);
-            bool have_fin = ok && wait_warp(ctl, &ctl->fin, 0, a.status);
+            const bool have_fin = ok && wait_warp(ctl, &ctl->fin, 0, a.status);
             bool have_o = false;
             if (have_fin && n_tiles > 0) {
                 have_o = wait_warp(ctl, &ctl->odone[(n_tiles - 1) & 1], ((n_tiles - 1) >> 1) & 1, a.status);
@@ -616,63 +664,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) sparse_
                 l = f.y;
             }
             const bool empty = !(l > 0.0f);
-            const bool write = h < a.h_q;
-            float inv = 0.0f;
+            const float lse2 = empty ? -INFINITY : m_ref + log2f(l);   // log2 units
+            float factor = 0.0f;
             if (!empty) {
                 float denom = l;
                 if (a.splits == 1 && a.sink != nullptr)
                     denom += exp2f(__ldg(a.sink + (h < a.h_q ? h : 0)) * kLog2e - m_ref);
-                inv = 1.0f / denom;
+                factor = 1.0f / denom;
             }
-            const bool use_o = have_o && !empty;
-            const int64_t rh = static_cast<int64_t>(row) * a.h_q + h;
-            if (a.splits == 1) {
-                __nv_bfloat16* dst = a.out + rh * 512;
-#pragma unroll 1
-                for (int c = 0; c < 16; ++c) {
-                    uint32_t o[32];
-                    if (have_o) {
-                        tmem_ld32(lane_base + kColO + 32 * c, o);
-                        tmem_wait_ld();
-                    }
-                    if (write) {
-#pragma unroll
-                        for (int v = 0; v < 4; ++v) {
-                            uint4 w;
-                            uint32_t* wp = reinterpret_cast<uint32_t*>(&w);
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const float x0 = use_o ? __uint_as_float(o[8 * v + 2 * e]) * inv : 0.0f;
-                                const float x1 = use_o ? __uint_as_float(o[8 * v + 2 * e + 1]) * inv : 0.0f;
-                                wp[e] = pack_bf16x2(x0, x1);
-                            }
-                            *reinterpret_cast<uint4*>(dst + 32 * c + 8 * v) = w;
-                        }
-                    }
-                }
-            } else {
-                const int64_t ph = (static_cast<int64_t>(row) * a.splits + split) * a.h_q + h;
-                float* dst = a.part_out + ph * 512;
-#pragma unroll 1
-                for (int c = 0; c < 16; ++c) {
-                    uint32_t o[32];
-                    if (have_o) {
-                        tmem_ld32(lane_base + kColO + 32 * c, o);
-                        tmem_wait_ld();
-                    }
-                    if (write) {
-#pragma unroll
-                        for (int v = 0; v < 8; ++v) {
-                            float4 w;
-                            w.x = use_o ? __uint_as_float(o[4 * v + 0]) * inv : 0.0f;
-                            w.y = use_o ? __uint_as_float(o[4 * v + 1]) * inv : 0.0f;
-                            w.z = use_o ? __uint_as_float(o[4 * v + 2]) * inv : 0.0f;
-                            w.w = use_o ? __uint_as_float(o[4 * v + 3]) * inv : 0.0f;
-                            *reinterpret_cast<float4*>(dst + 32 * c + 4 * v) = w;
-                        }
-                    }
-                }
+            if (h < a.h_q) {
+                if (a.splits == 1)
+                    a.lse[static_cast<int64_t>(row) * a.h_q + h] = lse2 * kLn2;
+                else
+                    a.part_lse[(static_cast<int64_t>(row) * a.splits + split) * a.h_q + h] = lse2;
             }
+            write_rows(a, smem, lane_base, have_o && !empty, factor, row, split, warp, lane, h);
         } else if (warp < 12) {
             // ============ CTA 1, warps 4-11: gather/dequant of the NoPE halves (V) ============
             gather_dequant<R, false, kVStages, kVTileBytes>(a, ctl, smem + kOffV, smem + kOffRaw1, ctl->vfull,
@@ -725,39 +731,40 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) sparse_
     }
 }
 
-// out = sum_p e^{lse_p - lse} out_p / (1 + e^{sink - lse}),  lse = ln sum_p e^{lse_p}
+// Split merge, one CTA per (query row, head), launched as a programmatic dependent of the
+// decode kernel: out = sum_s w_s part_s with w_s = 2^{lse2_s} / (sum_s 2^{lse2_s} + e^{sink}),
+// lse = ln sum_s e^{lse_s} (the sink is not part of lse). lse2 = log2-domain partial lse.
 __global__ void __launch_bounds__(128) combine_kernel(const float* __restrict__ part_out,
                                                       const float* __restrict__ part_lse, int splits, int h_q,
                                                       const float* __restrict__ sink, __nv_bfloat16* __restrict__ out,
                                                       float* __restrict__ lse) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");   // the decode grid's partials are visible
     const int rh = blockIdx.x;             // row * h_q + h
     const int row = rh / h_q;
     const int h = rh % h_q;
+    const int64_t base = static_cast<int64_t>(row) * splits;
     float m = -INFINITY;
-    for (int p = 0; p < splits; ++p) m = fmaxf(m, __ldg(part_lse + (static_cast<int64_t>(row) * splits + p) * h_q + h));
+    for (int p = 0; p < splits; ++p) m = fmaxf(m, part_lse[(base + p) * h_q + h]);
     const int d0 = threadIdx.x * 4;
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     float total = -INFINITY;
     if (m != -INFINITY) {
         float sum = 0.0f;
-        for (int p = 0; p < splits; ++p)
-            sum += expf(__ldg(part_lse + (static_cast<int64_t>(row) * splits + p) * h_q + h) - m);
-        total = m + logf(sum);
-        const float scale = 1.0f + (sink != nullptr ? expf(__ldg(sink + h) - total) : 0.0f);
+        for (int p = 0; p < splits; ++p) sum += exp2f(part_lse[(base + p) * h_q + h] - m);
+        total = (m + log2f(sum)) * kLn2;
+        const float inv = 1.0f / (sum + (sink != nullptr ? exp2f(__ldg(sink + h) * kLog2e - m) : 0.0f));
         for (int p = 0; p < splits; ++p) {
-            const int64_t ph = (static_cast<int64_t>(row) * splits + p) * h_q + h;
-            const float w = expf(__ldg(part_lse + ph) - total) / scale;
-            const float4 v = __ldg(reinterpret_cast<const float4*>(part_out + ph * 512 + d0));
-            acc[0] += w * v.x;
-            acc[1] += w * v.y;
-            acc[2] += w * v.z;
-            acc[3] += w * v.w;
+            const int64_t ph = (base + p) * h_q + h;
+            const float w = exp2f(part_lse[ph] - m) * inv;
+            const float4 v = *reinterpret_cast<const float4*>(part_out + ph * 512 + d0);
+            acc.x += w * v.x;
+            acc.y += w * v.y;
+            acc.z += w * v.z;
+            acc.w += w * v.w;
         }
     }
-    uint2 o;
-    o.x = pack_bf16x2(acc[0], acc[1]);
-    o.y = pack_bf16x2(acc[2], acc[3]);
-    *reinterpret_cast<uint2*>(out + static_cast<int64_t>(rh) * 512 + d0) = o;
+    *reinterpret_cast<uint2*>(out + static_cast<int64_t>(rh) * 512 + d0) =
+        make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
     if (threadIdx.x == 0) lse[rh] = total;
 }
 
@@ -806,9 +813,20 @@ cudaError_t launch_sparse_decode(const DecodeArgs& d, cudaStream_t stream) {
     }
     err = cudaGetLastError();
     if (err != cudaSuccess || d.splits == 1) return err;
-    combine_kernel<<<d.rows * d.h_q, 128, 0, stream>>>(d.part_out, d.part_lse, d.splits, d.h_q, d.attn_sink,
-                                                       static_cast<__nv_bfloat16*>(d.out), d.lse);
-    return cudaGetLastError();
+    // the merge launches while the decode grid runs and waits for it on the device
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(d.rows) * static_cast<unsigned>(d.h_q));
+    cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, combine_kernel, static_cast<const float*>(d.part_out),
+                              static_cast<const float*>(d.part_lse), d.splits, d.h_q, d.attn_sink,
+                              static_cast<__nv_bfloat16*>(d.out), d.lse);
 }
 
 }  // namespace nvfp4mla

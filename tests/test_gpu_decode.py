@@ -132,6 +132,40 @@ def test_zero_query_is_mean_of_values_and_splits_agree():
         assert torch.allclose(o, outs[0], atol=1e-2, rtol=1e-2)
 
 
+def test_many_splits_reused_dirty_workspace_is_deterministic():
+    """Five splits with a sink: the partials and their merge depend on nothing left in the
+    workspace, so a reused workspace and one filled with junk give the same bits, and those
+    match the oracle."""
+    rng = np.random.default_rng(4242)
+    B, H, topk, n_slots, splits, R = 3, 128, 640, 1000, 5, 352
+    q = rng.standard_normal((B, 1, H, 576)).astype(np.float32)
+    idx = np.stack([rng.choice(n_slots, size=topk, replace=False) for _ in range(B)]).reshape(B, 1, topk)
+    idx = idx.astype(np.int32)
+    idx[rng.random(idx.shape) < 0.1] = -1
+    sink = rng.standard_normal(H).astype(np.float32)
+    cache = fill_pool(lib.quantize_append, n_slots, R, 9, DEV)
+    qd = torch.from_numpy(q).to(torch.bfloat16).to(DEV)
+    idd = torch.from_numpy(idx).to(DEV)
+    sink_d = torch.from_numpy(sink).to(DEV)
+    ws = torch.zeros(lib.workspace_size(B, 1, H, topk, R, splits), dtype=torch.uint8, device=DEV)
+
+    def call():
+        out, lse = lib.sparse_mla_decode(qd, cache, idd, 0.05, attn_sink=sink_d, num_splits=splits, workspace=ws)
+        torch.cuda.synchronize()
+        return out.clone(), lse.clone()
+
+    first = call()
+    again = call()
+    ws.fill_(0x7F)
+    dirty = call()
+    for o, l in (again, dirty):
+        assert torch.equal(o, first[0]) and torch.equal(l, first[1])
+    recs = oracle_pool(9, n_slots, R)
+    ref_out, ref_lse = oracle.sparse_mla_decode(synth.bf16_bits(qd.cpu()), recs, idx.reshape(B, -1), 0.05,
+                                                attn_sink=sink)
+    assert_close(first[0], first[1], ref_out.reshape(B, 1, H, 512), ref_lse.reshape(B, 1, H))
+
+
 # ---- benchmark-sized workloads, sampled rows ---------------------------------------------
 
 def _sampled_parity(w: synth.DecodeWorkload, n_rows: int):
