@@ -284,6 +284,18 @@ __device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster
 __device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
 
 // 2^x, hardware approximation (relative error ~2^-22), denormal results flushed.
+// TMA tile::gather4: rows r0..r3 (x from element column x0) of a 2-D tensor map whose box is one
+// row high, into consecutive rows at dst_saddr (128-byte aligned); completion counted in bytes
+// on `bar`. Rows outside the tensor read the fill value (zeros).
+__device__ __forceinline__ void tma_gather4(uint32_t dst_saddr, const void* tmap, int32_t x0, int32_t r0, int32_t r1,
+                                            int32_t r2, int32_t r3, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst_saddr),
+        "l"(tmap), "r"(x0), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(smem_addr(bar))
+        : "memory");
+}
+
 // Packed fp32 pair arithmetic (one instruction for two lanes of a 64-bit register pair).
 __device__ __forceinline__ uint64_t f32x2_pack(float lo, float hi) {
     uint64_t r;

@@ -29,10 +29,13 @@
 //
 // Every wait is bounded: on timeout the CTA sets NVFP4_MLA_DEV_TIMEOUT, stops issuing work,
 // waits (bounded) for its MMAs to drain and frees its tensor memory before returning.
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
+#include <cstddef>
 #include <cstdint>
 
 #include "launch.h"
@@ -51,28 +54,29 @@ constexpr int kVStages = 2;                        // CTA 1: V tiles of 8 blocks
 constexpr int kVTileBytes = 8 * kBlkBytes;         // 64 KB
 constexpr int kPStages = 2;                        // CTA 1: P tiles [128 heads x 64 keys] bf16
 constexpr int kPBytes = kHeadsM * 128;             // 16 KB
-constexpr int kMaskSlots = 8;
-constexpr int kRawStages = 3;                      // raw records in flight (cp.async), in tiles
-// Raw record slot of one key: CTA 0 copies the whole record; CTA 1 the 256 NoPE bytes and the
-// 32 scale bytes (16-byte chunks 0..15 and 16..17 of the slot).
-template <int R, bool kWhole>
-struct RawSlot {
-    static constexpr int kChunks = kWhole ? R / 16 : 18;
-    static constexpr int kKeyBytes = kChunks * 16;
-    static constexpr int kTileBytes = kTile * kKeyBytes;
-    // record byte offset of slot chunk j
-    static __device__ __forceinline__ int src_offset(int j) {
-        return (kWhole || j < 16) ? 16 * j : (R == 352 ? 320 : 256) + 16 * (j - 16);
-    }
-    static constexpr int kScaleOffset = kWhole ? (R == 352 ? 320 : 256) : 256;
+constexpr int kMaskSlots = 16;
+// Raw-record ring, filled by TMA tile::gather4 (four whole records per instruction, each group of
+// four starting on a 128-byte boundary): CTA 0 keeps 3 tiles in flight for 352-byte records and
+// 2 for 432-byte records, CTA 1 keeps 2.
+template <int R>
+struct RawRing {
+    static constexpr int kGroupBytes = (4 * R + 127) / 128 * 128;   // 1408 | 1792
+    static constexpr int kTileBytes = 16 * kGroupBytes;             // 64 keys
+    static constexpr int kStages0 = R == 352 ? 3 : 2;
+    static constexpr int kStages1 = 2;
+    static __device__ __forceinline__ int key_offset(int key) { return (key >> 2) * kGroupBytes + (key & 3) * R; }
 };
-constexpr int kRaw0Bytes = kRawStages * kTile * 432;     // CTA 0 raw ring (largest record)
-constexpr int kRaw1Bytes = kRawStages * kTile * 288;     // CTA 1 raw ring
+constexpr int kProducerWarps = 2;
+constexpr int kMaxRawStages = 3;
 constexpr uint32_t kColS = 0;                      // CTA 0: S buffers [0,64), [64,128)
 constexpr uint32_t kColQ = 128;                    // CTA 0: Q, 576 bf16 = 288 columns
 constexpr uint32_t kColO = 0;                      // CTA 1: O, 512 columns
 constexpr int kTmemCols = 512;
-constexpr int kThreads = 448;
+constexpr int kThreads = 896;                      // 28 warps, roles below
+constexpr int kConvWarps = 16;                     // converter warps: 8 threads per key of a 64-key tile
+constexpr int kWarpConv0 = 8;                      // first converter warp
+constexpr int kWarpMma = 24;                       // QK issuers 24-25 (CTA 0), PV issuer 24 (CTA 1); TMEM owner
+constexpr int kWarpProd = 26;                      // producer warps 26-27
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;          // log2 units: rescale O only when max grows by > 2^8
@@ -85,7 +89,7 @@ struct __align__(8) SmemCtl {
     uint64_t kempty[kKStages];    // QK commit -> dequant
     uint64_t sfull[2];            // QK commit -> softmax
     uint64_t sfree[2];            // softmax has read S -> QK issuer
-    uint64_t mfull[kMaskSlots];   // used-key mask of a tile written
+    uint64_t mfull[kMaskSlots];   // used-key mask of a tile written (producer warps)
     uint64_t pempty[kPStages];    // CTA 1's PV has read the P slot (multicast commit)
     uint64_t qready;              // Q in TMEM
     // CTA 1
@@ -97,27 +101,41 @@ struct __align__(8) SmemCtl {
     uint64_t fin;                 // final (max, sum) of every row landed (tx-counted)
     // both
     uint64_t drain;
+    uint64_t rawfull[kMaxRawStages];    // producer warps: expect_tx + gather4 bytes -> converters
+    uint64_t rawempty[kMaxRawStages];   // converter warps (one arrival each) -> producers
+    uint32_t rawvalid[kMaxRawStages][2];   // used-key bits of the tile in each raw slot
+    uint32_t mask[kMaskSlots][2];          // CTA 0: used-key bits of tile i (slot i % kMaskSlots)
+    uint64_t xbar[2];             // CTA 0: both softmax halves posted their tile max (tile parity)
+    uint64_t lbar;                // CTA 0: softmax half 1 posted its final row sum
     uint32_t tmem_base;
     uint32_t abort;
-    uint8_t mask[kMaskSlots][8];
 };
 
 constexpr int kCtlBytes = 1024;
 static_assert(sizeof(SmemCtl) <= kCtlBytes, "control block");
 // CTA 0 data
 constexpr int kOffK = kCtlBytes;
-constexpr int kOffRaw0 = kOffK + kKStages * kKTileBytes;
 // CTA 1 data
 constexpr int kOffV = kCtlBytes;
 constexpr int kOffP = kOffV + kVStages * kVTileBytes;
 constexpr int kOffAlpha = kOffP + kPStages * kPBytes;          // [kPStages][128] fp32
 constexpr int kOffFin = kOffAlpha + kPStages * kHeadsM * 4;    // [128] (max, sum) pairs
-constexpr int kOffRaw1 = kOffFin + kHeadsM * 8;
-constexpr int kSmem0 = kOffRaw0 + kRaw0Bytes;
-constexpr int kSmem1 = kOffRaw1 + kRaw1Bytes;
-constexpr int kSmemBytes = 1024 + (kSmem0 > kSmem1 ? kSmem0 : kSmem1);
+constexpr int kOffRaw0 = kOffK + kKStages * kKTileBytes;        // CTA 0 raw ring
+constexpr int kOffRaw1 = kOffFin + kHeadsM * 8;                 // CTA 1 raw ring
+constexpr int kXchgBytes = (2 * 2 + 1) * kHeadsM * 4;          // CTA 0: [parity][half][128] maxima, [128] sums
+template <int R>
+struct SmemSize {
+    static constexpr int xchg0 = kOffRaw0 + RawRing<R>::kStages0 * RawRing<R>::kTileBytes;   // CTA 0 exchange
+    static constexpr int c0 = xchg0 + kXchgBytes;
+    static constexpr int c1 = kOffRaw1 + RawRing<R>::kStages1 * RawRing<R>::kTileBytes;
+    static constexpr int value = 1024 + (c0 > c1 ? c0 : c1);
+};
+static_assert(SmemSize<352>::value <= 232448 && SmemSize<432>::value <= 232448, "shared memory");
+static_assert(kOffRaw0 % 128 == 0 && kOffRaw1 % 128 == 0, "gather4 destinations are 128-byte aligned");
+static_assert(offsetof(SmemCtl, mask) % 8 == 0, "a tile's mask is read as one 64-bit word");
 
 struct KernelArgs {
+    CUtensorMap tmap;            // the cache as u32 [num_slots, R / 4], box one record
     const uint16_t* q;
     const uint8_t* cache;
     int64_t num_slots;
@@ -217,137 +235,173 @@ __device__ __forceinline__ int32_t load_index(const int32_t* idx_row, int pos, i
     return pos < key_end ? __ldg(idx_row + pos) : -1;
 }
 
-// Start the asynchronous copy of this thread's 16-byte chunks (j = q, q+4, ...) of one key's
-// raw record into its slot, or nothing for a masked key. Always commits a group, so the group
-// count stays one per tile.
-template <int R, bool kWhole>
-__device__ __forceinline__ void issue_raw(const KernelArgs& a, int32_t index, uint32_t slot_saddr, int q) {
-    using S = RawSlot<R, kWhole>;
-    if (index >= 0 && index < a.num_slots) {
-        const uint8_t* rec = a.cache + static_cast<int64_t>(index) * R;
-#pragma unroll
-        for (int j = q; j < S::kChunks; j += 4) cp_async16(slot_saddr + 16 * j, rec + S::src_offset(j));
-    }
-    cp_async_commit();
-}
-
-// Convert this thread's part of one key from its raw slot into the bf16 tile: the 16-wide NoPE
-// blocks 4c+q (c = 0..7) and, with kRope, RoPE dims [16q, 16q+16). A masked key writes zeros.
+// Convert this thread's part of one key from its raw record in shared memory into the bf16
+// tile. Eight threads share a key: thread (q, hi) = (sub & 3, sub >> 2) converts the 16-wide NoPE
+// blocks 4c+q for c = 4hi..4hi+3 (their four scales are bytes 8q+4hi.. of the permuted scale field
+// of a 352-byte record: one 4-byte load) and RoPE dims [8 sub, 8 sub + 8). A masked key writes
+// zeros.
 template <int R, bool kRope>
-__device__ __forceinline__ void convert_part(const uint8_t* slot, bool valid, uint8_t* tile, int key, int q) {
-    using S = RawSlot<R, kRope>;
+__device__ __forceinline__ void convert_part(const uint8_t* rec, bool valid, uint8_t* tile, int key, int sub) {
+    const int q = sub & 3;
+    const int hi = sub >> 2;
     if (valid) {
-        uint32_t sw[8];
+        uint32_t sw;   // four scale bytes, block 4(4hi + j) + q in byte j
         if constexpr (R == 352) {
-            // blocks 4c+q have their scales at bytes 8q + c of the scale field (permuted layout):
-            // one 8-byte load
-            const uint2 s8 = *reinterpret_cast<const uint2*>(slot + S::kScaleOffset + 8 * q);
-#pragma unroll
-            for (int c = 0; c < 8; ++c) sw[c] = ((c < 4 ? s8.x : s8.y) >> (8 * (c & 3))) & 0xFFu;
+            sw = *reinterpret_cast<const uint32_t*>(rec + 320 + 8 * q + 4 * hi);
         } else {
-            const uint4 s0 = *reinterpret_cast<const uint4*>(slot + S::kScaleOffset);
-            const uint4 s1 = *reinterpret_cast<const uint4*>(slot + S::kScaleOffset + 16);
-            const uint32_t w[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+            // natural order: block b at byte 256 + b
+            const uint32_t* s32 = reinterpret_cast<const uint32_t*>(rec + 256);
+            sw = 0u;
 #pragma unroll
-            for (int c = 0; c < 8; ++c) sw[c] = (w[c] >> (8 * q)) & 0xFFu;   // byte 4c + q
+            for (int j = 0; j < 4; ++j) sw |= ((s32[4 * hi + j] >> (8 * q)) & 0xFFu) << (8 * j);
         }
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-            const uint2 codes = *reinterpret_cast<const uint2*>(slot + 32 * c + 8 * q);
-            uint4 lo, hi;
-            dq_block(codes, sw[c], lo, hi);
+        for (int j = 0; j < 4; ++j) {
+            const int c = 4 * hi + j;
+            const uint2 codes = *reinterpret_cast<const uint2*>(rec + 32 * c + 8 * q);
+            uint4 lo, hv;
+            dq_block(codes, (sw >> (8 * j)) & 0xFFu, lo, hv);
             *reinterpret_cast<uint4*>(tile + c * kBlkBytes + swz(key, 2 * q)) = lo;
-            *reinterpret_cast<uint4*>(tile + c * kBlkBytes + swz(key, 2 * q + 1)) = hi;
+            *reinterpret_cast<uint4*>(tile + c * kBlkBytes + swz(key, 2 * q + 1)) = hv;
         }
         if constexpr (kRope) {
-            uint4 r0, r1;
+            uint4 r;
             if constexpr (R == 352) {
-                const uint4 e = *reinterpret_cast<const uint4*>(slot + 256 + 16 * q);
-                r0 = make_uint4(dq_e4m3x2(e.x), dq_e4m3x2(e.x >> 16), dq_e4m3x2(e.y), dq_e4m3x2(e.y >> 16));
-                r1 = make_uint4(dq_e4m3x2(e.z), dq_e4m3x2(e.z >> 16), dq_e4m3x2(e.w), dq_e4m3x2(e.w >> 16));
+                const uint2 e = *reinterpret_cast<const uint2*>(rec + 256 + 8 * sub);
+                r = make_uint4(dq_e4m3x2(e.x), dq_e4m3x2(e.x >> 16), dq_e4m3x2(e.y), dq_e4m3x2(e.y >> 16));
             } else {
-                r0 = *reinterpret_cast<const uint4*>(slot + 304 + 32 * q);
-                r1 = *reinterpret_cast<const uint4*>(slot + 304 + 32 * q + 16);
+                r = *reinterpret_cast<const uint4*>(rec + 304 + 16 * sub);
             }
-            *reinterpret_cast<uint4*>(tile + 8 * kBlkBytes + swz(key, 2 * q)) = r0;
-            *reinterpret_cast<uint4*>(tile + 8 * kBlkBytes + swz(key, 2 * q + 1)) = r1;
+            *reinterpret_cast<uint4*>(tile + 8 * kBlkBytes + swz(key, sub)) = r;
         }
     } else {
         const uint4 z = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-        for (int c = 0; c < (kRope ? 9 : 8); ++c) {
+        for (int j = 0; j < 4; ++j) {
+            const int c = 4 * hi + j;
             *reinterpret_cast<uint4*>(tile + c * kBlkBytes + swz(key, 2 * q)) = z;
             *reinterpret_cast<uint4*>(tile + c * kBlkBytes + swz(key, 2 * q + 1)) = z;
         }
+        if constexpr (kRope) *reinterpret_cast<uint4*>(tile + 8 * kBlkBytes + swz(key, sub)) = z;
     }
 }
 
-// Gather/dequant warps (256 threads, t = 0..255): 4 threads per key, one 64-key tile per
-// iteration. Raw records are copied with cp.async kRawStages tiles ahead into a ring of raw
-// slots; each iteration waits for its own tile's copies, then converts into stage
-// i % kStages of `ring` once the consumer released it (`empty`), and arrives on `full`.
-// With kRope (CTA 0: whole records, RoPE included) the used-key mask of each tile is also
-// published (mask ring + mfull) and K stages are only written once Q has left them (qready).
-template <int R, bool kRope, int kStages, int kStageBytes>
-__device__ __forceinline__ void gather_dequant(const KernelArgs& a, SmemCtl* ctl, uint8_t* ring, uint8_t* raw,
-                                               uint64_t* full, uint64_t* empty, const int32_t* idx_row,
-                                               int key_begin, int key_end, int n_tiles, int t) {
-    using S = RawSlot<R, kRope>;
-    const int key = t >> 2;
-    const int q = t & 3;
-    const int wq = t >> 5;
-    const int lane = t & 31;
-    auto pos_of = [&](int i) { return key_begin + kTile * i + key; };
-    const uint32_t raw_key = smem_addr(raw) + key * S::kKeyBytes;
-    int32_t ix[kRawStages + 1];
+// Producer warps (kProducerWarps of them, pw = 0, 1): lane l < 8 of warp pw owns group
+// g = 8 pw + l, keys 4g..4g+3 of every tile. For tile j the warp publishes its 32 used-key bits,
+// registers the bytes it will gather on rawfull[j % kRaw] and issues one TMA gather4 per group
+// with a used key (a masked row re-fetches a used row of its group, so every coordinate lies
+// inside the cache; its bytes are never read), once the converters released the raw slot.
+// Indices are read one tile ahead. Out-of-range indices are masked (CTA 0 reports them). Before
+// returning, the warp waits for every gather it started.
+template <int R, bool kRope, int kRaw>
+__device__ __forceinline__ void produce_raw(const KernelArgs& a, SmemCtl* ctl, uint8_t* raw, const int32_t* idx_row,
+                                            int key_begin, int key_end, int n_tiles, int pw, int lane) {
+    using RR = RawRing<R>;
+    const int g = 8 * pw + (lane & 7);
+    auto load4 = [&](int j, int32_t (&r)[4]) {
 #pragma unroll
-    for (int k = 0; k < kRawStages; ++k) {
-        ix[k] = load_index(idx_row, pos_of(k), key_end);
-        issue_raw<R, kRope>(a, k < n_tiles ? ix[k] : -1, raw_key + k * S::kTileBytes, q);
+        for (int m = 0; m < 4; ++m) {
+            const int pos = key_begin + kTile * j + 4 * g + m;
+            r[m] = (lane < 8 && pos < key_end) ? __ldg(idx_row + pos) : -1;
+        }
+    };
+    int32_t nxt[4];
+    load4(0, nxt);
+    int issued = 0;
+    for (int j = 0; j < n_tiles; ++j) {
+        const int rs = j % kRaw;
+        int32_t r[4] = {nxt[0], nxt[1], nxt[2], nxt[3]};
+        if (j + 1 < n_tiles) load4(j + 1, nxt);
+        if (j >= kRaw && !wait_warp(ctl, &ctl->rawempty[rs], ((j / kRaw) - 1) & 1, a.status)) break;
+        uint32_t bits = 0;
+        int32_t first = -1;
+#pragma unroll
+        for (int m = 3; m >= 0; --m) {
+            const bool ok = r[m] >= 0 && r[m] < a.num_slots;
+            if (kRope && a.status != nullptr && r[m] >= a.num_slots) atomicOr(a.status, 0x2u);
+            bits |= (ok ? 1u : 0u) << m;
+            if (ok) first = r[m];
+        }
+#pragma unroll
+        for (int m = 0; m < 4; ++m)
+            if (!((bits >> m) & 1u)) r[m] = first;
+        const uint32_t word = __reduce_or_sync(0xffffffffu, lane < 8 ? bits << (4 * lane) : 0u);
+        const uint32_t groups = __popc(__ballot_sync(0xffffffffu, lane < 8 && bits != 0u));
+        if (lane == 0) {
+            ctl->rawvalid[rs][pw] = word;
+            if (kRope) {
+                ctl->mask[j % kMaskSlots][pw] = word;
+                mbar_arrive(&ctl->mfull[j % kMaskSlots]);
+            }
+            mbar_arrive_expect_tx(&ctl->rawfull[rs], groups * 4u * R);
+        }
+        __syncwarp();
+        if (lane < 8 && bits != 0u)
+            tma_gather4(smem_addr(raw + rs * RR::kTileBytes + g * RR::kGroupBytes), &a.tmap, 0, r[0], r[1], r[2], r[3],
+                        &ctl->rawfull[rs]);
+        issued = j + 1;
     }
-    ix[kRawStages] = load_index(idx_row, pos_of(kRawStages), key_end);
+    // only after a timeout can gathers still be in flight here; they must land before the CTA exits
+    for (int j = issued - 1; j >= 0 && j >= issued - kRaw; --j) mbar_wait(&ctl->rawfull[j % kRaw], (j / kRaw) & 1);
+}
+
+// Converter warps (kConvWarps of them, t = 0..511): eight threads per key, one 64-key tile per
+// iteration. Waits for tile i's records in raw slot i % kRaw, converts them into stage
+// i % kStages of `ring` once the consumer released it (`empty`), arrives on `full` and hands the
+// raw slot back. With kRope (CTA 0) the K stages are written only after Q has left them (qready).
+template <int R, bool kRope, int kStages, int kStageBytes, int kRaw>
+__device__ __forceinline__ void convert_tiles(const KernelArgs& a, SmemCtl* ctl, uint8_t* ring, uint8_t* raw,
+                                              uint64_t* full, uint64_t* empty, int n_tiles, int t) {
+    using RR = RawRing<R>;
+    const int key = t >> 3;
+    const int sub = t & 7;
+    const int lane = t & 31;
     for (int i = 0; i < n_tiles; ++i) {
         const int ks = i % kStages;
-        const int rs = i % kRawStages;
-        const int32_t index = ix[0];
-        if (kRope && q == 0 && index >= a.num_slots && a.status != nullptr) atomicOr(a.status, 0x2u);
-        const bool valid = index >= 0 && index < a.num_slots;
-        cp_async_wait<kRawStages - 1>();      // this thread's copies of tile i have landed
-        __syncwarp();                          // ... and those of the 3 other threads of its key
+        const int rs = i % kRaw;
+        if (!wait_warp(ctl, &ctl->rawfull[rs], (i / kRaw) & 1, a.status)) break;
         if (i >= kStages && !wait_warp(ctl, &empty[ks], ((i - kStages) / kStages) & 1, a.status)) break;
         if (kRope && i == 0 && !wait_warp(ctl, &ctl->qready, 0, a.status)) break;   // K stages held Q
-        convert_part<R, kRope>(raw + rs * S::kTileBytes + key * S::kKeyBytes, valid, ring + ks * kStageBytes, key, q);
-        if constexpr (kRope) {
-            const uint32_t used = __ballot_sync(0xffffffffu, valid);
-            if (lane == 0) {
-                uint32_t m = 0;
-#pragma unroll
-                for (int k = 0; k < 8; ++k) m |= ((used >> (4 * k)) & 1u) << k;
-                ctl->mask[i % kMaskSlots][wq] = static_cast<uint8_t>(m);
-                mbar_arrive(&ctl->mfull[i % kMaskSlots]);
-            }
-        }
+        const bool valid = ((ctl->rawvalid[rs][key >> 5] >> (key & 31)) & 1u) != 0u;
+        convert_part<R, kRope>(raw + rs * RR::kTileBytes + RR::key_offset(key), valid, ring + ks * kStageBytes, key, sub);
         fence_proxy_async_smem();
         mbar_arrive(&full[ks]);
-        // the raw slot of tile i is free: start tile i + kRawStages there
         __syncwarp();
-        const int nx = i + kRawStages;
-        issue_raw<R, kRope>(a, nx < n_tiles ? ix[kRawStages] : -1, raw_key + rs * S::kTileBytes, q);
-#pragma unroll
-        for (int k = 0; k < kRawStages; ++k) ix[k] = ix[k + 1];
-        ix[kRawStages] = load_index(idx_row, pos_of(nx + 1), key_end);
+        if (lane == 0) mbar_arrive(&ctl->rawempty[rs]);
     }
-    cp_async_wait<0>();
 }
 
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t threads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
-// CTA 1, warps 0-3 (thread h = TMEM lane h): O * factor for the row's 128 x 512 block, written
-// out (bf16 `out` when there is one split, fp32 partial otherwise) through shared memory so
-// that every warp store covers whole 128-byte lines. Four quarters of 128 columns, staged in
-// the two V stages alternately (row h at h * 512, 16-byte chunk k at slot k ^ (h & 7)).
+// Output of CTA 1: O * factor for the row's 128 x 512 block goes out (bf16 `out` when there is
+// one split, fp32 partial otherwise) through shared memory, so every warp store covers whole
+// 128-byte lines. Four quarters of 128 columns are staged in the two V stages alternately (row h
+// at h * 512, 16-byte chunk k at slot k ^ (h & 7)) by warps 0-3 (thread h = TMEM lane h), and
+// copied out by those warps and the converter warps together (kOutWarps warps, one row per warp
+// instruction); one named barrier per quarter orders staging and copying.
+constexpr int kOutWarps = 4 + kConvWarps;
+
+__device__ __forceinline__ void copy_quarter(const KernelArgs& a, const uint8_t* buf, int qt, int row, int split,
+                                             int wi, int lane) {
+    if (a.splits == 1) {
+#pragma unroll 2
+        for (int hh = wi; hh < a.h_q; hh += kOutWarps) {
+            const float4 x = *reinterpret_cast<const float4*>(buf + hh * 512 + ((lane ^ (hh & 7)) << 4));
+            *reinterpret_cast<uint2*>(a.out + (static_cast<int64_t>(row) * a.h_q + hh) * 512 + 128 * qt + 4 * lane) =
+                make_uint2(pack_bf16x2(x.x, x.y), pack_bf16x2(x.z, x.w));
+        }
+    } else {
+        float* base = a.part_out + (static_cast<int64_t>(row) * a.splits + split) * a.h_q * 512 + 128 * qt + 4 * lane;
+#pragma unroll 2
+        for (int hh = wi; hh < a.h_q; hh += kOutWarps)
+            *reinterpret_cast<float4*>(base + static_cast<int64_t>(hh) * 512) =
+                *reinterpret_cast<const float4*>(buf + hh * 512 + ((lane ^ (hh & 7)) << 4));
+    }
+}
+
+// Warps 0-3: stage each quarter, then copy their share.
 __device__ __forceinline__ void write_rows(const KernelArgs& a, uint8_t* smem, uint32_t lane_base, bool use_o,
                                            float factor, int row, int split, int warp, int lane, int h) {
 #pragma unroll 1
@@ -370,32 +424,23 @@ __device__ __forceinline__ void write_rows(const KernelArgs& a, uint8_t* smem, u
                 *reinterpret_cast<float4*>(buf + h * 512 + (((8 * c + v) ^ (h & 7)) << 4)) = w;
             }
         }
-        named_bar_sync(1, 128);
-        const int nrows = min(32, a.h_q - 32 * warp);
-        if (a.splits == 1) {
-            __nv_bfloat16* dst = a.out + (static_cast<int64_t>(row) * a.h_q + 32 * warp) * 512 + 128 * qt + 4 * lane;
-#pragma unroll 4
-            for (int r = 0; r < nrows; ++r) {
-                const int hh = 32 * warp + r;
-                const float4 x = *reinterpret_cast<const float4*>(buf + hh * 512 + ((lane ^ (hh & 7)) << 4));
-                *reinterpret_cast<uint2*>(dst + static_cast<int64_t>(r) * 512) =
-                    make_uint2(pack_bf16x2(x.x, x.y), pack_bf16x2(x.z, x.w));
-            }
-        } else {
-            float* dst = a.part_out + ((static_cast<int64_t>(row) * a.splits + split) * a.h_q + 32 * warp) * 512 +
-                         128 * qt + 4 * lane;
-#pragma unroll 4
-            for (int r = 0; r < nrows; ++r) {
-                const int hh = 32 * warp + r;
-                *reinterpret_cast<float4*>(dst + static_cast<int64_t>(r) * 512) =
-                    *reinterpret_cast<const float4*>(buf + hh * 512 + ((lane ^ (hh & 7)) << 4));
-            }
-        }
+        named_bar_sync(1, 32 * kOutWarps);
+        copy_quarter(a, buf, qt, row, split, warp, lane);
+    }
+}
+
+// Converter warps of CTA 1, once their tiles are done: copy their share of each quarter.
+__device__ __forceinline__ void help_write_rows(const KernelArgs& a, const uint8_t* smem, int row, int split, int wi,
+                                                int lane) {
+#pragma unroll 1
+    for (int qt = 0; qt < 4; ++qt) {
+        named_bar_sync(1, 32 * kOutWarps);
+        copy_quarter(a, smem + kOffV + (qt & 1) * kVTileBytes, qt, row, split, wi, lane);
     }
 }
 
 template <int R>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) sparse_decode_kernel(const KernelArgs a) {
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) sparse_decode_kernel(const __grid_constant__ KernelArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     SmemCtl* ctl = reinterpret_cast<SmemCtl*>(smem);
@@ -413,29 +458,35 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) sparse_
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kKStages; ++i) {
-            mbar_init(&ctl->kfull[i], 256);
+            mbar_init(&ctl->kfull[i], 32 * kConvWarps);
             mbar_init(&ctl->kempty[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&ctl->sfull[i], 1);
-            mbar_init(&ctl->sfree[i], 128);
-            mbar_init(&ctl->vfull[i], 256);
+            mbar_init(&ctl->sfree[i], 256);
+            mbar_init(&ctl->vfull[i], 32 * kConvWarps);
             mbar_init(&ctl->vempty[i], 1);
             mbar_init(&ctl->odone[i], 1);
+            mbar_init(&ctl->xbar[i], 256);
         }
-        for (int i = 0; i < kMaskSlots; ++i) mbar_init(&ctl->mfull[i], 8);
+        for (int i = 0; i < kMaskSlots; ++i) mbar_init(&ctl->mfull[i], kProducerWarps);
+        for (int i = 0; i < kMaxRawStages; ++i) {
+            mbar_init(&ctl->rawfull[i], kProducerWarps);
+            mbar_init(&ctl->rawempty[i], kConvWarps);
+        }
         for (int i = 0; i < kPStages; ++i) {
             mbar_init(&ctl->pempty[i], 1);
             mbar_init(&ctl->pfull[i], 4);
             mbar_init(&ctl->ready[i], 128);
         }
-        mbar_init(&ctl->qready, 128);
+        mbar_init(&ctl->qready, 256);
+        mbar_init(&ctl->lbar, 128);
         mbar_init(&ctl->fin, 4);
         mbar_init(&ctl->drain, crank == 0 ? 2 : 1);
         ctl->abort = 0u;
         fence_barrier_init();
     }
-    if (warp == 12) {
+    if (warp == kWarpMma) {
         tmem_alloc(&ctl->tmem_base, kTmemCols);
         tmem_relinquish();
     }
@@ -449,29 +500,37 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) sparse_
     // others at exit.
     cluster_arrive();
 
+    const bool converter = warp >= kWarpConv0 && warp < kWarpConv0 + kConvWarps;
+    const int conv_t = threadIdx.x - 32 * kWarpConv0;
     if (crank == 0) {
         // Q [128 x 576] bf16 is staged through the two K stages (exactly 144 KB) with coalesced
-        // loads by every thread; row h's 16-byte chunk c sits at h*1152 + (c ^ (h & 7))*16 so the
-        // row reads below are conflict-free. The K stages are written only after qready.
+        // loads by warps 0..kWarpProd-1 (the producer warps start gathering meanwhile); row h's
+        // 16-byte chunk c sits at h*1152 + (c ^ (h & 7))*16 so the row reads below are
+        // conflict-free. The K stages are written only after qready.
         uint8_t* sQ = smem + kOffK;
-        {
+        if (warp < kWarpProd) {
             const uint4* src = reinterpret_cast<const uint4*>(a.q + static_cast<int64_t>(row) * a.h_q * kDqk);
-            for (int g = threadIdx.x; g < kHeadsM * (kDqk / 8); g += kThreads) {
+            for (int g = threadIdx.x; g < kHeadsM * (kDqk / 8); g += 32 * kWarpProd) {
                 const int hh = g / (kDqk / 8), c = g % (kDqk / 8);
                 uint4 x = make_uint4(0u, 0u, 0u, 0u);
                 if (hh < a.h_q) x = __ldg(src + g);
                 *reinterpret_cast<uint4*>(sQ + hh * (kDqk * 2) + ((c ^ (hh & 7)) << 4)) = x;
             }
+            named_bar_sync(1, 32 * kWarpProd);
         }
-        __syncthreads();
-        if (warp < 4) {
-            // ============ CTA 0, warps 0-3: Q into TMEM, then the softmax ============
-            const int h = threadIdx.x;
-            const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+        if (warp < 8) {
+            // ============ CTA 0, warps 0-7: Q into TMEM, then the softmax ============
+            // Warp w serves TMEM lanes 32 (w & 3) .. +31 (thread = head h) and score columns
+            // [32 half, 32 half + 32) of each tile, half = w >> 2. The halves exchange their tile
+            // maxima (xbar) so both rescale identically, and merge their row sums at the end.
+            const int quad = warp & 3;
+            const int half = warp >> 2;
+            const int h = quad * 32 + lane;
+            const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
             {
                 const uint8_t* qrow = sQ + h * (kDqk * 2);
 #pragma unroll 1
-                for (int c = 0; c < 9; ++c) {          // 9 x 64 dims = 9 x 32 columns
+                for (int c = half ? 5 : 0; c < (half ? 9 : 5); ++c) {   // 9 x 64 dims = 9 x 32 columns
                     uint32_t v[32];
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
@@ -494,62 +553,69 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) sparse_
             const uint32_t peer_fin = mapa_shared(smem_addr(smem + kOffFin) + 8 * h, 1);
             const uint32_t peer_pfull0 = mapa_shared(smem_addr(&ctl->pfull[0]), 1);
             const uint32_t peer_finbar = mapa_shared(smem_addr(&ctl->fin), 1);
-            float m_ref = -INFINITY;   // reference max, log2 units of scaled logits
-            float l = 0.0f;            // sum of 2^(s - m_ref) over used keys
+            float* xmax = reinterpret_cast<float*>(smem + SmemSize<R>::xchg0);   // [parity][half][128]
+            float* xsum = xmax + 4 * kHeadsM;                                      // [128]
+            float m_ref = -INFINITY;   // reference max, log2 units of scaled logits (same in both halves)
+            float l = 0.0f;            // this half's sum of 2^(z - m_ref) over used keys
             bool ok = true;
             for (int i = 0; i < n_tiles && ok; ++i) {
                 const int b = i & 1;
                 ok = wait_warp(ctl, &ctl->sfull[b], (i >> 1) & 1, a.status);
                 if (!ok) break;
                 tc_fence_after_sync();
-                uint32_t s[64];
-                tmem_ld32(lane_base + kColS + 64 * b, *reinterpret_cast<uint32_t(*)[32]>(s));
-                tmem_ld32(lane_base + kColS + 64 * b + 32, *reinterpret_cast<uint32_t(*)[32]>(s + 32));
+                uint32_t s[32];
+                tmem_ld32(lane_base + kColS + 64 * b + 32 * half, s);
                 tmem_wait_ld();
                 tc_fence_before_sync();
                 mbar_arrive(&ctl->sfree[b]);
                 ok = wait_warp(ctl, &ctl->mfull[i % kMaskSlots], (i / kMaskSlots) & 1, a.status);
                 if (!ok) break;
-                const uint64_t used = *reinterpret_cast<const volatile uint64_t*>(ctl->mask[i % kMaskSlots]);
+                const uint32_t used = *reinterpret_cast<const volatile uint32_t*>(&ctl->mask[i % kMaskSlots][half]);
                 // ---- online softmax (log2 domain, lazy reference max): z = s * scale_log2.
                 // Common case (every key used, scale > 0): the max is taken on the raw scores and
                 // each z - m is one fused multiply-add; otherwise masked keys become -inf first.
                 float zs = a.scale_log2;      // multiplier applied to s[] below
-                float tile_max;
-                if (used == ~0ull && zs > 0.0f) {
+                float part_max;
+                if (used == 0xFFFFFFFFu && zs > 0.0f) {
                     float m0 = -INFINITY, m1 = -INFINITY;
 #pragma unroll
-                    for (int j = 0; j < 64; j += 4) {
+                    for (int j = 0; j < 32; j += 4) {
                         m0 = fmax3(m0, __uint_as_float(s[j]), __uint_as_float(s[j + 1]));
                         m1 = fmax3(m1, __uint_as_float(s[j + 2]), __uint_as_float(s[j + 3]));
                     }
-                    tile_max = fmaxf(m0, m1) * zs;
+                    part_max = fmaxf(m0, m1) * zs;
                 } else {
                     float m0 = -INFINITY, m1 = -INFINITY;
 #pragma unroll
-                    for (int j = 0; j < 64; j += 2) {
-                        const float v0 = ((used >> j) & 1ull) ? __uint_as_float(s[j]) * zs : -INFINITY;
-                        const float v1 = ((used >> (j + 1)) & 1ull) ? __uint_as_float(s[j + 1]) * zs : -INFINITY;
+                    for (int j = 0; j < 32; j += 2) {
+                        const float v0 = ((used >> j) & 1u) ? __uint_as_float(s[j]) * zs : -INFINITY;
+                        const float v1 = ((used >> (j + 1)) & 1u) ? __uint_as_float(s[j + 1]) * zs : -INFINITY;
                         s[j] = __float_as_uint(v0);
                         s[j + 1] = __float_as_uint(v1);
                         m0 = fmaxf(m0, v0);
                         m1 = fmaxf(m1, v1);
                     }
-                    tile_max = fmaxf(m0, m1);
+                    part_max = fmaxf(m0, m1);
                     zs = 1.0f;
                 }
+                // ---- tile max over both halves
+                xmax[(b * 2 + half) * kHeadsM + h] = part_max;
+                mbar_arrive(&ctl->xbar[b]);
+                ok = wait_warp(ctl, &ctl->xbar[b], (i >> 1) & 1, a.status);
+                if (!ok) break;
+                const float tile_max = fmaxf(part_max, xmax[(b * 2 + (half ^ 1)) * kHeadsM + h]);
                 float alpha = 1.0f;
                 if (tile_max > m_ref + kRescaleThreshold) {
                     if (m_ref != -INFINITY) alpha = ex2_approx(m_ref - tile_max);
                     m_ref = tile_max;
                 }
-                uint32_t p[32];
+                uint32_t p[16];
                 if (m_ref != -INFINITY) {
                     const uint64_t mul2 = f32x2_pack(zs, zs);
                     const uint64_t neg_m2 = f32x2_pack(-m_ref, -m_ref);
                     uint64_t la = f32x2_pack(0.0f, 0.0f), lb = la;
 #pragma unroll
-                    for (int j = 0; j < 64; j += 4) {
+                    for (int j = 0; j < 32; j += 4) {
                         const float2 z0 = f32x2_unpack(
                             f32x2_fma(f32x2_pack(__uint_as_float(s[j]), __uint_as_float(s[j + 1])), mul2, neg_m2));
                         const float2 z1 = f32x2_unpack(
@@ -565,9 +631,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) sparse_
                     l = l * alpha + ((sa.x + sa.y) + (sb.x + sb.y));
                 } else {
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) p[j] = 0u;
+                    for (int j = 0; j < 16; ++j) p[j] = 0u;
                 }
-                // ---- P row h and alpha -> CTA 1's slot (i % kPStages), once its PV released it
+                // ---- this half of P row h (and alpha) -> CTA 1's slot (i % kPStages), once its PV released it
                 const int ps = i % kPStages;
                 if (i >= kPStages) {
                     ok = wait_warp(ctl, &ctl->pempty[ps], ((i / kPStages) - 1) & 1, a.status);
@@ -576,25 +642,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) sparse_
                 const uint32_t dst = peer_p + ps * kPBytes;
                 const uint32_t bar = peer_pfull0 + 8 * ps;
 #pragma unroll
-                for (int c = 0; c < 8; ++c)
-                    st_async_u4(dst + ((c ^ (h & 7)) << 4),
+                for (int c = 0; c < 4; ++c)
+                    st_async_u4(dst + (((4 * half + c) ^ (h & 7)) << 4),
                                 make_uint4(p[4 * c], p[4 * c + 1], p[4 * c + 2], p[4 * c + 3]), bar);
-                st_async_f32(peer_alpha + ps * kHeadsM * 4, alpha, bar);
+                if (half == 0) st_async_f32(peer_alpha + ps * kHeadsM * 4, alpha, bar);
             }
-            // ---- running max and sum to CTA 1, which writes out and lse
-            if (ok) st_async_v2(peer_fin, m_ref, l, peer_finbar);
-        } else if (warp < 12) {
-            // ============ CTA 0, warps 4-11: gather/dequant of whole records ============
-            gather_dequant<R, true, kKStages, kKTileBytes>(a, ctl, smem + kOffK, smem + kOffRaw0, ctl->kfull,
-                                                           ctl->kempty, idx_row, key_begin, key_end, n_tiles,
-                                                           threadIdx.x - 128);
+            // ---- running max and the merged row sum to CTA 1, which writes out and lse
+            if (half == 1) {
+                xsum[h] = l;
+                mbar_arrive(&ctl->lbar);
+            } else if (ok && wait_warp(ctl, &ctl->lbar, 0, a.status)) {
+                st_async_v2(peer_fin, m_ref, l + xsum[h], peer_finbar);
+            }
+        } else if (converter) {
+            // ============ CTA 0, warps 8-23: dequant of whole records (K tiles) ============
+            convert_tiles<R, true, kKStages, kKTileBytes, RawRing<R>::kStages0>(
+                a, ctl, smem + kOffK, smem + kOffRaw0, ctl->kfull, ctl->kempty, n_tiles, conv_t);
+        } else if (warp >= kWarpProd) {
+            // ============ CTA 0, warps 26-27: record gathers (TMA gather4) ============
+            produce_raw<R, true, RawRing<R>::kStages0>(a, ctl, smem + kOffRaw0, idx_row, key_begin, key_end, n_tiles,
+                                                       warp - kWarpProd, lane);
         } else {
-            // ============ CTA 0, warps 12-13: QK issuers (warp 12 even tiles, warp 13 odd tiles) ============
+            // ============ CTA 0, warps 24-25: QK issuers (warp 24 even tiles, warp 25 odd tiles) ============
             const uint32_t idesc_qk = idesc_bf16_f32(kHeadsM, kTile, false, false);
             const uint64_t kdesc0 = sdesc_sw128(smem_addr(smem + kOffK), 16, 1024);
             const bool leader = elect_one_in_warp();
             bool ok = wait_warp(ctl, &ctl->qready, 0, a.status);
-            for (int i = warp - 12; i < n_tiles && ok; i += 2) {
+            for (int i = warp - kWarpMma; i < n_tiles && ok; i += 2) {
                 const int ks = i % kKStages;
                 const int b = i & 1;
                 ok = wait_warp(ctl, &ctl->kfull[ks], (i / kKStages) & 1, a.status);
@@ -679,13 +753,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) sparse_
                     a.part_lse[(static_cast<int64_t>(row) * a.splits + split) * a.h_q + h] = lse2;
             }
             write_rows(a, smem, lane_base, have_o && !empty, factor, row, split, warp, lane, h);
-        } else if (warp < 12) {
-            // ============ CTA 1, warps 4-11: gather/dequant of the NoPE halves (V) ============
-            gather_dequant<R, false, kVStages, kVTileBytes>(a, ctl, smem + kOffV, smem + kOffRaw1, ctl->vfull,
-                                                            ctl->vempty, idx_row, key_begin, key_end, n_tiles,
-                                                            threadIdx.x - 128);
-        } else if (warp == 12) {
-            // ============ CTA 1, warp 12: PV issuer (warp 13 idle) ============
+        } else if (converter) {
+            // ============ CTA 1, warps 8-23: dequant of the NoPE halves (V tiles) ============
+            convert_tiles<R, false, kVStages, kVTileBytes, RawRing<R>::kStages1>(
+                a, ctl, smem + kOffV, smem + kOffRaw1, ctl->vfull, ctl->vempty, n_tiles, conv_t);
+            help_write_rows(a, smem, row, split, 4 + warp - kWarpConv0, lane);
+        } else if (warp >= kWarpProd) {
+            // ============ CTA 1, warps 26-27: record gathers (TMA gather4) ============
+            produce_raw<R, false, RawRing<R>::kStages1>(a, ctl, smem + kOffRaw1, idx_row, key_begin, key_end, n_tiles,
+                                                        warp - kWarpProd, lane);
+        } else if (warp == kWarpMma) {
+            // ============ CTA 1, warp 24: PV issuer (warps 4-7 and 25 idle) ============
             cluster_wait();          // CTA 0's pempty barriers exist before the first multicast commit
             const uint32_t idesc_pv = idesc_bf16_f32(kHeadsM, 256, false, true);
             const uint64_t pdesc0 = sdesc_sw128(smem_addr(smem + kOffP), 16, 1024);
@@ -703,11 +781,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) sparse_
                     const uint64_t pd = pdesc0 + static_cast<uint64_t>((ps * kPBytes) >> 4);
                     const uint64_t vd = vdesc0 + static_cast<uint64_t>((vs * kVTileBytes) >> 4);
 #pragma unroll
-                    for (int half = 0; half < 2; ++half)
+                    for (int nh = 0; nh < 2; ++nh)
 #pragma unroll
                         for (int kk = 0; kk < kTile / 16; ++kk)
-                            mma_ss(tmem + kColO + 256 * half, pd + ((kk * 32) >> 4),
-                                   vd + ((half * 4 * kBlkBytes + kk * 2048) >> 4), idesc_pv, (i > 0 || kk > 0) ? 1u : 0u);
+                            mma_ss(tmem + kColO + 256 * nh, pd + ((kk * 32) >> 4),
+                                   vd + ((nh * 4 * kBlkBytes + kk * 2048) >> 4), idesc_pv, (i > 0 || kk > 0) ? 1u : 0u);
                     mma_commit(&ctl->vempty[vs]);
                     mma_commit(&ctl->odone[i & 1]);
                     mma_commit_multicast(&ctl->pempty[ps], 0x1);
@@ -721,51 +799,67 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) sparse_
     }
 
     // threads that have not waited on the prologue's cluster phase do so now
-    const bool waited = (crank == 0 && warp < 4) || (crank == 1 && warp == 12);
+    const bool waited = (crank == 0 && warp < 8) || (crank == 1 && warp == kWarpMma);
     if (!waited) cluster_wait();
     tc_fence_before_sync();
     cluster_sync();          // no CTA leaves while its peer may still touch its shared memory
-    if (warp == 12) {
+    if (warp == kWarpMma) {
         tc_fence_after_sync();
         tmem_dealloc(tmem, kTmemCols);
     }
 }
 
-// Split merge, one CTA per (query row, head), launched as a programmatic dependent of the
-// decode kernel: out = sum_s w_s part_s with w_s = 2^{lse2_s} / (sum_s 2^{lse2_s} + e^{sink}),
-// lse = ln sum_s e^{lse_s} (the sink is not part of lse). lse2 = log2-domain partial lse.
-__global__ void __launch_bounds__(128) combine_kernel(const float* __restrict__ part_out,
+// Split merge, one warp per (query row, head), 8 per CTA, launched as a programmatic dependent of
+// the decode kernel: out = sum_s w_s part_s with w_s = 2^{lse2_s} / (sum_s 2^{lse2_s} + e^{sink}),
+// lse = ln sum_s e^{lse_s} (the sink is not part of lse); lse2 = log2-domain partial lse. Lane s
+// holds splits s and s + 32; lane l accumulates columns 4l + 128k (k = 0..3).
+__global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ part_out,
                                                       const float* __restrict__ part_lse, int splits, int h_q,
-                                                      const float* __restrict__ sink, __nv_bfloat16* __restrict__ out,
-                                                      float* __restrict__ lse) {
+                                                      int rows_heads, const float* __restrict__ sink,
+                                                      __nv_bfloat16* __restrict__ out, float* __restrict__ lse) {
     asm volatile("griddepcontrol.wait;" ::: "memory");   // the decode grid's partials are visible
-    const int rh = blockIdx.x;             // row * h_q + h
+    const int lane = threadIdx.x & 31;
+    const int rh = blockIdx.x * 8 + (threadIdx.x >> 5);   // row * h_q + h
+    if (rh >= rows_heads) return;
     const int row = rh / h_q;
     const int h = rh % h_q;
     const int64_t base = static_cast<int64_t>(row) * splits;
-    float m = -INFINITY;
-    for (int p = 0; p < splits; ++p) m = fmaxf(m, part_lse[(base + p) * h_q + h]);
-    const int d0 = threadIdx.x * 4;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    const float v0 = lane < splits ? part_lse[(base + lane) * h_q + h] : -INFINITY;
+    const float v1 = lane + 32 < splits ? part_lse[(base + lane + 32) * h_q + h] : -INFINITY;
+    float m = fmaxf(v0, v1);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    float4 acc[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
     float total = -INFINITY;
     if (m != -INFINITY) {
-        float sum = 0.0f;
-        for (int p = 0; p < splits; ++p) sum += exp2f(part_lse[(base + p) * h_q + h] - m);
+        const float e0 = exp2f(v0 - m), e1 = exp2f(v1 - m);
+        float sum = e0 + e1;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
         total = (m + log2f(sum)) * kLn2;
         const float inv = 1.0f / (sum + (sink != nullptr ? exp2f(__ldg(sink + h) * kLog2e - m) : 0.0f));
-        for (int p = 0; p < splits; ++p) {
-            const int64_t ph = (base + p) * h_q + h;
-            const float w = exp2f(part_lse[ph] - m) * inv;
-            const float4 v = *reinterpret_cast<const float4*>(part_out + ph * 512 + d0);
-            acc.x += w * v.x;
-            acc.y += w * v.y;
-            acc.z += w * v.z;
-            acc.w += w * v.w;
+        const float w0 = e0 * inv, w1 = e1 * inv;
+        for (int sp = 0; sp < splits; ++sp) {
+            const float w = __shfl_sync(0xffffffffu, sp < 32 ? w0 : w1, sp & 31);
+            const float* src = part_out + ((base + sp) * h_q + h) * 512 + 4 * lane;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float4 v = *reinterpret_cast<const float4*>(src + 128 * k);
+                acc[k].x += w * v.x;
+                acc[k].y += w * v.y;
+                acc[k].z += w * v.z;
+                acc[k].w += w * v.w;
+            }
         }
     }
-    *reinterpret_cast<uint2*>(out + static_cast<int64_t>(rh) * 512 + d0) =
-        make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
-    if (threadIdx.x == 0) lse[rh] = total;
+    __nv_bfloat16* dst = out + static_cast<int64_t>(rh) * 512 + 4 * lane;
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+        *reinterpret_cast<uint2*>(dst + 128 * k) =
+            make_uint2(pack_bf16x2(acc[k].x, acc[k].y), pack_bf16x2(acc[k].z, acc[k].w));
+    if (lane == 0) lse[rh] = total;
 }
 
 }  // namespace
@@ -775,9 +869,60 @@ int decode_keys_per_split(int topk, int splits) {
     return (per + kTile - 1) / kTile * kTile;
 }
 
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no libcuda link).
+EncodeTiledFn encode_tiled() {
+    static const EncodeTiledFn fn = [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            p = nullptr;
+        return reinterpret_cast<EncodeTiledFn>(p);
+    }();
+    return fn;
+}
+
+// The cache as a 2-D tensor of u32 [rows, R / 4] whose box is one record, for tile::gather4.
+// Rows are capped at 2^31 - 1 (indices are int32); an empty cache maps one row that is never
+// fetched (no index is in range).
+bool encode_cache_map(CUtensorMap* map, const uint8_t* cache, int64_t num_slots, int record_bytes) {
+    const EncodeTiledFn fn = encode_tiled();
+    if (fn == nullptr) return false;
+    const int64_t rows = num_slots < 1 ? 1 : (num_slots > 0x7FFFFFFF ? 0x7FFFFFFF : num_slots);
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(record_bytes / 4), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(record_bytes)};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(record_bytes / 4), 1u};
+    const cuuint32_t elem_strides[2] = {1u, 1u};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint8_t*>(cache), dims, strides, box, elem_strides,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Raises the kernel's dynamic shared memory limit once per device.
+template <int R>
+cudaError_t prepare_kernel() {
+    static std::atomic<uint64_t> done{0};
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    const uint64_t bit = dev < 64 ? (uint64_t(1) << dev) : 0;
+    if (bit != 0 && (done.load(std::memory_order_relaxed) & bit)) return cudaSuccess;
+    err = cudaFuncSetAttribute(sparse_decode_kernel<R>, cudaFuncAttributeMaxDynamicSharedMemorySize, SmemSize<R>::value);
+    if (err == cudaSuccess && bit != 0) done.fetch_or(bit, std::memory_order_relaxed);
+    return err;
+}
+
+}  // namespace
+
 cudaError_t launch_sparse_decode(const DecodeArgs& d, cudaStream_t stream) {
-    static bool attr_done[2] = {false, false};
     KernelArgs a;
+    if (!encode_cache_map(&a.tmap, d.cache, d.num_slots, d.record_bytes)) return cudaErrorInvalidValue;
     a.q = static_cast<const uint16_t*>(d.q);
     a.cache = d.cache;
     a.num_slots = d.num_slots;
@@ -797,26 +942,21 @@ cudaError_t launch_sparse_decode(const DecodeArgs& d, cudaStream_t stream) {
     const dim3 block(kThreads);
     cudaError_t err;
     if (d.record_bytes == 352) {
-        if (!attr_done[0]) {
-            err = cudaFuncSetAttribute(sparse_decode_kernel<352>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-            if (err != cudaSuccess) return err;
-            attr_done[0] = true;
-        }
-        sparse_decode_kernel<352><<<grid, block, kSmemBytes, stream>>>(a);
+        err = prepare_kernel<352>();
+        if (err != cudaSuccess) return err;
+        sparse_decode_kernel<352><<<grid, block, SmemSize<352>::value, stream>>>(a);
     } else {
-        if (!attr_done[1]) {
-            err = cudaFuncSetAttribute(sparse_decode_kernel<432>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-            if (err != cudaSuccess) return err;
-            attr_done[1] = true;
-        }
-        sparse_decode_kernel<432><<<grid, block, kSmemBytes, stream>>>(a);
+        err = prepare_kernel<432>();
+        if (err != cudaSuccess) return err;
+        sparse_decode_kernel<432><<<grid, block, SmemSize<432>::value, stream>>>(a);
     }
     err = cudaGetLastError();
     if (err != cudaSuccess || d.splits == 1) return err;
     // the merge launches while the decode grid runs and waits for it on the device
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(d.rows) * static_cast<unsigned>(d.h_q));
-    cfg.blockDim = dim3(128);
+    const int rows_heads = d.rows * d.h_q;
+    cfg.gridDim = dim3(static_cast<unsigned>((rows_heads + 7) / 8));
+    cfg.blockDim = dim3(256);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -825,7 +965,7 @@ cudaError_t launch_sparse_decode(const DecodeArgs& d, cudaStream_t stream) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, combine_kernel, static_cast<const float*>(d.part_out),
-                              static_cast<const float*>(d.part_lse), d.splits, d.h_q, d.attn_sink,
+                              static_cast<const float*>(d.part_lse), d.splits, d.h_q, rows_heads, d.attn_sink,
                               static_cast<__nv_bfloat16*>(d.out), d.lse);
 }
 
