@@ -241,48 +241,58 @@ __device__ __forceinline__ int32_t load_index(const int32_t* idx_row, int pos, i
 // of a 352-byte record: one 4-byte load) and RoPE dims [8 sub, 8 sub + 8). A masked key writes
 // zeros.
 template <int R, bool kRope>
-__device__ __forceinline__ void convert_part(const uint8_t* rec, bool valid, uint8_t* tile, int key, int sub) {
+__device__ __forceinline__ void convert_part(uint32_t rec, bool valid, uint32_t tile, int key, int sub) {
     const int q = sub & 3;
     const int hi = sub >> 2;
     if (valid) {
+        // all shared-memory reads first (they are issued back to back), then convert and store
+        uint2 codes[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) codes[j] = lds_u64(rec + 32 * (4 * hi + j) + 8 * q);
         uint32_t sw;   // four scale bytes, block 4(4hi + j) + q in byte j
         if constexpr (R == 352) {
-            sw = *reinterpret_cast<const uint32_t*>(rec + 320 + 8 * q + 4 * hi);
+            sw = lds_u32(rec + 320 + 8 * q + 4 * hi);
         } else {
             // natural order: block b at byte 256 + b
-            const uint32_t* s32 = reinterpret_cast<const uint32_t*>(rec + 256);
+            const uint4 s4 = lds_u128(rec + 256 + 16 * hi);
+            const uint32_t w[4] = {s4.x, s4.y, s4.z, s4.w};
             sw = 0u;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) sw |= ((s32[4 * hi + j] >> (8 * q)) & 0xFFu) << (8 * j);
+            for (int j = 0; j < 4; ++j) sw |= ((w[j] >> (8 * q)) & 0xFFu) << (8 * j);
+        }
+        uint4 rope = make_uint4(0u, 0u, 0u, 0u);
+        if constexpr (kRope) {
+            if constexpr (R == 352) {
+                const uint2 e = lds_u64(rec + 256 + 8 * sub);
+                rope.x = e.x;
+                rope.y = e.y;
+            } else {
+                rope = lds_u128(rec + 304 + 16 * sub);
+            }
         }
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             const int c = 4 * hi + j;
-            const uint2 codes = *reinterpret_cast<const uint2*>(rec + 32 * c + 8 * q);
             uint4 lo, hv;
-            dq_block(codes, (sw >> (8 * j)) & 0xFFu, lo, hv);
-            *reinterpret_cast<uint4*>(tile + c * kBlkBytes + swz(key, 2 * q)) = lo;
-            *reinterpret_cast<uint4*>(tile + c * kBlkBytes + swz(key, 2 * q + 1)) = hv;
+            dq_block(codes[j], (sw >> (8 * j)) & 0xFFu, lo, hv);
+            sts_u128(tile + c * kBlkBytes + swz(key, 2 * q), lo);
+            sts_u128(tile + c * kBlkBytes + swz(key, 2 * q + 1), hv);
         }
         if constexpr (kRope) {
-            uint4 r;
-            if constexpr (R == 352) {
-                const uint2 e = *reinterpret_cast<const uint2*>(rec + 256 + 8 * sub);
-                r = make_uint4(dq_e4m3x2(e.x), dq_e4m3x2(e.x >> 16), dq_e4m3x2(e.y), dq_e4m3x2(e.y >> 16));
-            } else {
-                r = *reinterpret_cast<const uint4*>(rec + 304 + 16 * sub);
-            }
-            *reinterpret_cast<uint4*>(tile + 8 * kBlkBytes + swz(key, sub)) = r;
+            uint4 r = rope;
+            if constexpr (R == 352)
+                r = make_uint4(dq_e4m3x2(rope.x), dq_e4m3x2(rope.x >> 16), dq_e4m3x2(rope.y), dq_e4m3x2(rope.y >> 16));
+            sts_u128(tile + 8 * kBlkBytes + swz(key, sub), r);
         }
     } else {
         const uint4 z = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             const int c = 4 * hi + j;
-            *reinterpret_cast<uint4*>(tile + c * kBlkBytes + swz(key, 2 * q)) = z;
-            *reinterpret_cast<uint4*>(tile + c * kBlkBytes + swz(key, 2 * q + 1)) = z;
+            sts_u128(tile + c * kBlkBytes + swz(key, 2 * q), z);
+            sts_u128(tile + c * kBlkBytes + swz(key, 2 * q + 1), z);
         }
-        if constexpr (kRope) *reinterpret_cast<uint4*>(tile + 8 * kBlkBytes + swz(key, sub)) = z;
+        if constexpr (kRope) sts_u128(tile + 8 * kBlkBytes + swz(key, sub), z);
     }
 }
 
@@ -356,6 +366,8 @@ __device__ __forceinline__ void convert_tiles(const KernelArgs& a, SmemCtl* ctl,
     const int key = t >> 3;
     const int sub = t & 7;
     const int lane = t & 31;
+    const uint32_t raw_s = smem_addr(raw);
+    const uint32_t ring_s = smem_addr(ring);
     for (int i = 0; i < n_tiles; ++i) {
         const int ks = i % kStages;
         const int rs = i % kRaw;
@@ -363,7 +375,8 @@ __device__ __forceinline__ void convert_tiles(const KernelArgs& a, SmemCtl* ctl,
         if (i >= kStages && !wait_warp(ctl, &empty[ks], ((i - kStages) / kStages) & 1, a.status)) break;
         if (kRope && i == 0 && !wait_warp(ctl, &ctl->qready, 0, a.status)) break;   // K stages held Q
         const bool valid = ((ctl->rawvalid[rs][key >> 5] >> (key & 31)) & 1u) != 0u;
-        convert_part<R, kRope>(raw + rs * RR::kTileBytes + RR::key_offset(key), valid, ring + ks * kStageBytes, key, sub);
+        convert_part<R, kRope>(raw_s + rs * RR::kTileBytes + RR::key_offset(key), valid, ring_s + ks * kStageBytes,
+                               key, sub);
         fence_proxy_async_smem();
         mbar_arrive(&full[ks]);
         __syncwarp();
@@ -385,19 +398,20 @@ constexpr int kOutWarps = 4 + kConvWarps;
 
 __device__ __forceinline__ void copy_quarter(const KernelArgs& a, const uint8_t* buf, int qt, int row, int split,
                                              int wi, int lane) {
+    const uint32_t b = smem_addr(buf);
     if (a.splits == 1) {
 #pragma unroll 2
         for (int hh = wi; hh < a.h_q; hh += kOutWarps) {
-            const float4 x = *reinterpret_cast<const float4*>(buf + hh * 512 + ((lane ^ (hh & 7)) << 4));
+            const uint4 x = lds_u128(b + hh * 512 + ((lane ^ (hh & 7)) << 4));
             *reinterpret_cast<uint2*>(a.out + (static_cast<int64_t>(row) * a.h_q + hh) * 512 + 128 * qt + 4 * lane) =
-                make_uint2(pack_bf16x2(x.x, x.y), pack_bf16x2(x.z, x.w));
+                make_uint2(pack_bf16x2(__uint_as_float(x.x), __uint_as_float(x.y)),
+                           pack_bf16x2(__uint_as_float(x.z), __uint_as_float(x.w)));
         }
     } else {
         float* base = a.part_out + (static_cast<int64_t>(row) * a.splits + split) * a.h_q * 512 + 128 * qt + 4 * lane;
 #pragma unroll 2
         for (int hh = wi; hh < a.h_q; hh += kOutWarps)
-            *reinterpret_cast<float4*>(base + static_cast<int64_t>(hh) * 512) =
-                *reinterpret_cast<const float4*>(buf + hh * 512 + ((lane ^ (hh & 7)) << 4));
+            *reinterpret_cast<uint4*>(base + static_cast<int64_t>(hh) * 512) = lds_u128(b + hh * 512 + ((lane ^ (hh & 7)) << 4));
     }
 }
 
@@ -416,12 +430,12 @@ __device__ __forceinline__ void write_rows(const KernelArgs& a, uint8_t* smem, u
             }
 #pragma unroll
             for (int v = 0; v < 8; ++v) {
-                float4 w;
-                w.x = use_o ? __uint_as_float(o[4 * v + 0]) * factor : 0.0f;
-                w.y = use_o ? __uint_as_float(o[4 * v + 1]) * factor : 0.0f;
-                w.z = use_o ? __uint_as_float(o[4 * v + 2]) * factor : 0.0f;
-                w.w = use_o ? __uint_as_float(o[4 * v + 3]) * factor : 0.0f;
-                *reinterpret_cast<float4*>(buf + h * 512 + (((8 * c + v) ^ (h & 7)) << 4)) = w;
+                uint4 w;
+                w.x = __float_as_uint(use_o ? __uint_as_float(o[4 * v + 0]) * factor : 0.0f);
+                w.y = __float_as_uint(use_o ? __uint_as_float(o[4 * v + 1]) * factor : 0.0f);
+                w.z = __float_as_uint(use_o ? __uint_as_float(o[4 * v + 2]) * factor : 0.0f);
+                w.w = __float_as_uint(use_o ? __uint_as_float(o[4 * v + 3]) * factor : 0.0f);
+                sts_u128(smem_addr(buf) + h * 512 + (((8 * c + v) ^ (h & 7)) << 4), w);
             }
         }
         named_bar_sync(1, 32 * kOutWarps);
@@ -442,7 +456,9 @@ __device__ __forceinline__ void help_write_rows(const KernelArgs& a, const uint8
 template <int R>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) sparse_decode_kernel(const __grid_constant__ KernelArgs a) {
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // 1024-byte aligned base, computed as an offset into the shared array so that every access
+    // through `smem` stays a shared-memory access
+    uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     SmemCtl* ctl = reinterpret_cast<SmemCtl*>(smem);
 
     const int crank = static_cast<int>(cluster_ctarank());   // 0: QK + softmax, 1: PV
