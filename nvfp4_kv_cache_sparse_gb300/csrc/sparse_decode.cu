@@ -230,11 +230,6 @@ __device__ __forceinline__ bool wait_warp(SmemCtl* ctl, uint64_t* bar, uint32_t 
     return __all_sync(0xffffffffu, ok);
 }
 
-// Index of this thread's key (or -1 past the end of the split).
-__device__ __forceinline__ int32_t load_index(const int32_t* idx_row, int pos, int key_end) {
-    return pos < key_end ? __ldg(idx_row + pos) : -1;
-}
-
 // Convert this thread's part of one key from its raw record in shared memory into the bf16
 // tile. Eight threads share a key: thread (q, hi) = (sub & 3, sub >> 2) converts the 16-wide NoPE
 // blocks 4c+q for c = 4hi..4hi+3 (their four scales are bytes 8q+4hi.. of the permuted scale field
@@ -391,17 +386,24 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t threads) {
 // Output of CTA 1: O * factor for the row's 128 x 512 block goes out (bf16 `out` when there is
 // one split, fp32 partial otherwise) through shared memory, so every warp store covers whole
 // 128-byte lines. Four quarters of 128 columns are staged in the two V stages alternately (row h
-// at h * 512, 16-byte chunk k at slot k ^ (h & 7)) by warps 0-3 (thread h = TMEM lane h), and
-// copied out by those warps and the converter warps together (kOutWarps warps, one row per warp
-// instruction); one named barrier per quarter orders staging and copying.
-constexpr int kOutWarps = 4 + kConvWarps;
+// at h * 512, 16-byte chunk k at slot k ^ (h & 7)) by warps 0-3 (thread h = TMEM lane h) and
+// copied out by the converter warps (one row per warp instruction), so staging of a quarter
+// overlaps the copy of the previous one. Named barriers: kBarFull + b (staged -> copy) and
+// kBarEmpty + b (copied -> restage), b = quarter & 1, each counting all kOutThreads threads.
+constexpr int kOutThreads = 128 + 32 * kConvWarps;
+constexpr uint32_t kBarFull = 2;
+constexpr uint32_t kBarEmpty = 4;
+
+__device__ __forceinline__ void named_bar_arrive(uint32_t id, uint32_t threads) {
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
 
 __device__ __forceinline__ void copy_quarter(const KernelArgs& a, const uint8_t* buf, int qt, int row, int split,
                                              int wi, int lane) {
     const uint32_t b = smem_addr(buf);
     if (a.splits == 1) {
 #pragma unroll 2
-        for (int hh = wi; hh < a.h_q; hh += kOutWarps) {
+        for (int hh = wi; hh < a.h_q; hh += kConvWarps) {
             const uint4 x = lds_u128(b + hh * 512 + ((lane ^ (hh & 7)) << 4));
             *reinterpret_cast<uint2*>(a.out + (static_cast<int64_t>(row) * a.h_q + hh) * 512 + 128 * qt + 4 * lane) =
                 make_uint2(pack_bf16x2(__uint_as_float(x.x), __uint_as_float(x.y)),
@@ -410,17 +412,17 @@ __device__ __forceinline__ void copy_quarter(const KernelArgs& a, const uint8_t*
     } else {
         float* base = a.part_out + (static_cast<int64_t>(row) * a.splits + split) * a.h_q * 512 + 128 * qt + 4 * lane;
 #pragma unroll 2
-        for (int hh = wi; hh < a.h_q; hh += kOutWarps)
+        for (int hh = wi; hh < a.h_q; hh += kConvWarps)
             *reinterpret_cast<uint4*>(base + static_cast<int64_t>(hh) * 512) = lds_u128(b + hh * 512 + ((lane ^ (hh & 7)) << 4));
     }
 }
 
-// Warps 0-3: stage each quarter, then copy their share.
-__device__ __forceinline__ void write_rows(const KernelArgs& a, uint8_t* smem, uint32_t lane_base, bool use_o,
-                                           float factor, int row, int split, int warp, int lane, int h) {
+// Warps 0-3: stage each quarter once the copy of the quarter before last has left its buffer.
+__device__ __forceinline__ void write_rows(uint8_t* smem, uint32_t lane_base, bool use_o, float factor, int h) {
 #pragma unroll 1
     for (int qt = 0; qt < 4; ++qt) {
-        uint8_t* buf = smem + kOffV + (qt & 1) * kVTileBytes;
+        const uint32_t buf = smem_addr(smem + kOffV + (qt & 1) * kVTileBytes);
+        if (qt >= 2) named_bar_sync(kBarEmpty + (qt & 1), kOutThreads);
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
             uint32_t o[32];
@@ -435,21 +437,21 @@ __device__ __forceinline__ void write_rows(const KernelArgs& a, uint8_t* smem, u
                 w.y = __float_as_uint(use_o ? __uint_as_float(o[4 * v + 1]) * factor : 0.0f);
                 w.z = __float_as_uint(use_o ? __uint_as_float(o[4 * v + 2]) * factor : 0.0f);
                 w.w = __float_as_uint(use_o ? __uint_as_float(o[4 * v + 3]) * factor : 0.0f);
-                sts_u128(smem_addr(buf) + h * 512 + (((8 * c + v) ^ (h & 7)) << 4), w);
+                sts_u128(buf + h * 512 + (((8 * c + v) ^ (h & 7)) << 4), w);
             }
         }
-        named_bar_sync(1, 32 * kOutWarps);
-        copy_quarter(a, buf, qt, row, split, warp, lane);
+        named_bar_arrive(kBarFull + (qt & 1), kOutThreads);
     }
 }
 
-// Converter warps of CTA 1, once their tiles are done: copy their share of each quarter.
+// Converter warps of CTA 1, once their tiles are done: copy each quarter out as it is staged.
 __device__ __forceinline__ void help_write_rows(const KernelArgs& a, const uint8_t* smem, int row, int split, int wi,
                                                 int lane) {
 #pragma unroll 1
     for (int qt = 0; qt < 4; ++qt) {
-        named_bar_sync(1, 32 * kOutWarps);
+        named_bar_sync(kBarFull + (qt & 1), kOutThreads);
         copy_quarter(a, smem + kOffV + (qt & 1) * kVTileBytes, qt, row, split, wi, lane);
+        if (qt < 2) named_bar_arrive(kBarEmpty + (qt & 1), kOutThreads);
     }
 }
 
@@ -768,12 +770,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) sparse_
                 else
                     a.part_lse[(static_cast<int64_t>(row) * a.splits + split) * a.h_q + h] = lse2;
             }
-            write_rows(a, smem, lane_base, have_o && !empty, factor, row, split, warp, lane, h);
+            write_rows(smem, lane_base, have_o && !empty, factor, h);
         } else if (converter) {
             // ============ CTA 1, warps 8-23: dequant of the NoPE halves (V tiles) ============
             convert_tiles<R, false, kVStages, kVTileBytes, RawRing<R>::kStages1>(
                 a, ctl, smem + kOffV, smem + kOffRaw1, ctl->vfull, ctl->vempty, n_tiles, conv_t);
-            help_write_rows(a, smem, row, split, 4 + warp - kWarpConv0, lane);
+            help_write_rows(a, smem, row, split, warp - kWarpConv0, lane);
         } else if (warp >= kWarpProd) {
             // ============ CTA 1, warps 26-27: record gathers (TMA gather4) ============
             produce_raw<R, false, RawRing<R>::kStages1>(a, ctl, smem + kOffRaw1, idx_row, key_begin, key_end, n_tiles,
