@@ -316,6 +316,16 @@ __device__ __forceinline__ void tma_gather4(uint32_t dst_saddr, const void* tmap
         : "memory");
 }
 
+// TMA 2-D tiled load of the box at element coordinates (x, y) into dst_saddr; completion counted
+// in bytes on `bar`.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst_saddr, const void* tmap, int32_t x, int32_t y, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
+            "r"(dst_saddr),
+        "l"(tmap), "r"(x), "r"(y), "r"(smem_addr(bar))
+        : "memory");
+}
+
 // Packed fp32 pair arithmetic (one instruction for two lanes of a 64-bit register pair).
 __device__ __forceinline__ uint64_t f32x2_pack(float lo, float hi) {
     uint64_t r;

@@ -91,6 +91,7 @@ struct __align__(8) SmemCtl {
     uint64_t sfree[2];            // softmax has read S -> QK issuer
     uint64_t mfull[kMaskSlots];   // used-key mask of a tile written (producer warps)
     uint64_t pempty[kPStages];    // CTA 1's PV has read the P slot (multicast commit)
+    uint64_t qload;               // CTA 0: Q's nine 64-column boxes landed in shared memory (TMA)
     uint64_t qready;              // Q in TMEM
     // CTA 1
     uint64_t vfull[kVStages];     // dequant -> PV issuer
@@ -136,6 +137,7 @@ static_assert(offsetof(SmemCtl, mask) % 8 == 0, "a tile's mask is read as one 64
 
 struct KernelArgs {
     CUtensorMap tmap;            // the cache as u32 [num_slots, R / 4], box one record
+    CUtensorMap qmap;            // q as bf16 [rows * h_q, 576], box 64 columns x 128 heads, 128B swizzle
     const uint16_t* q;
     const uint8_t* cache;
     int64_t num_slots;
@@ -497,6 +499,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) sparse_
             mbar_init(&ctl->pfull[i], 4);
             mbar_init(&ctl->ready[i], 128);
         }
+        mbar_init(&ctl->qload, 1);
         mbar_init(&ctl->qready, 256);
         mbar_init(&ctl->lbar, 128);
         mbar_init(&ctl->fin, 4);
@@ -521,20 +524,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) sparse_
     const bool converter = warp >= kWarpConv0 && warp < kWarpConv0 + kConvWarps;
     const int conv_t = threadIdx.x - 32 * kWarpConv0;
     if (crank == 0) {
-        // Q [128 x 576] bf16 is staged through the two K stages (exactly 144 KB) with coalesced
-        // loads by warps 0..kWarpProd-1 (the producer warps start gathering meanwhile); row h's
-        // 16-byte chunk c sits at h*1152 + (c ^ (h & 7))*16 so the row reads below are
-        // conflict-free. The K stages are written only after qready.
+        // Q [128 x 576] bf16 is staged through the two K stages (exactly 144 KB) by nine TMA box
+        // loads (64 columns x 128 heads each, 128B-swizzled: head h's 16-byte chunk c of box b at
+        // b*16384 + (h >> 3)*1024 + (h & 7)*128 + (c ^ (h & 7))*16, so the row reads below are
+        // conflict-free). Heads past the last query row read zeros. The K stages are written only
+        // after qready.
         uint8_t* sQ = smem + kOffK;
-        if (warp < kWarpProd) {
-            const uint4* src = reinterpret_cast<const uint4*>(a.q + static_cast<int64_t>(row) * a.h_q * kDqk);
-            for (int g = threadIdx.x; g < kHeadsM * (kDqk / 8); g += 32 * kWarpProd) {
-                const int hh = g / (kDqk / 8), c = g % (kDqk / 8);
-                uint4 x = make_uint4(0u, 0u, 0u, 0u);
-                if (hh < a.h_q) x = __ldg(src + g);
-                *reinterpret_cast<uint4*>(sQ + hh * (kDqk * 2) + ((c ^ (hh & 7)) << 4)) = x;
-            }
-            named_bar_sync(1, 32 * kWarpProd);
+        if (threadIdx.x == 32 * kWarpMma) {
+            mbar_arrive_expect_tx(&ctl->qload, 9u * 16384u);
+            for (int bx = 0; bx < 9; ++bx)
+                tma_load_2d(smem_addr(sQ + bx * 16384), &a.qmap, 64 * bx, row * a.h_q, &ctl->qload);
         }
         if (warp < 8) {
             // ============ CTA 0, warps 0-7: Q into TMEM, then the softmax ============
@@ -546,13 +545,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) sparse_
             const int h = quad * 32 + lane;
             const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
             {
-                const uint8_t* qrow = sQ + h * (kDqk * 2);
+                const bool have_q = wait_warp(ctl, &ctl->qload, 0, a.status);
+                const uint32_t q_s = smem_addr(sQ) + (h >> 3) * 1024 + (h & 7) * 128;
 #pragma unroll 1
                 for (int c = half ? 5 : 0; c < (half ? 9 : 5); ++c) {   // 9 x 64 dims = 9 x 32 columns
                     uint32_t v[32];
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
-                        const uint4 x = *reinterpret_cast<const uint4*>(qrow + (((8 * c + j) ^ (h & 7)) << 4));
+                        const uint4 x = have_q ? lds_u128(q_s + c * 16384 + ((j ^ (h & 7)) << 4)) : make_uint4(0u, 0u, 0u, 0u);
                         v[4 * j] = x.x;
                         v[4 * j + 1] = x.y;
                         v[4 * j + 2] = x.z;
@@ -922,6 +922,20 @@ bool encode_cache_map(CUtensorMap* map, const uint8_t* cache, int64_t num_slots,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// q as a 2-D tensor of bf16 [rows * h_q, 576], box 64 columns x 128 heads with the 128B swizzle;
+// heads past the end read zeros.
+bool encode_q_map(CUtensorMap* map, const void* q, int64_t heads) {
+    const EncodeTiledFn fn = encode_tiled();
+    if (fn == nullptr || heads < 1 || heads > 0x7FFFFFFF) return false;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kDqk), static_cast<cuuint64_t>(heads)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kDqk) * 2u};
+    const cuuint32_t box[2] = {64u, 128u};
+    const cuuint32_t elem_strides[2] = {1u, 1u};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(q), dims, strides, box, elem_strides,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Raises the kernel's dynamic shared memory limit once per device.
 template <int R>
 cudaError_t prepare_kernel() {
@@ -941,6 +955,7 @@ cudaError_t prepare_kernel() {
 cudaError_t launch_sparse_decode(const DecodeArgs& d, cudaStream_t stream) {
     KernelArgs a;
     if (!encode_cache_map(&a.tmap, d.cache, d.num_slots, d.record_bytes)) return cudaErrorInvalidValue;
+    if (!encode_q_map(&a.qmap, d.q, static_cast<int64_t>(d.rows) * d.h_q)) return cudaErrorInvalidValue;
     a.q = static_cast<const uint16_t*>(d.q);
     a.cache = d.cache;
     a.num_slots = d.num_slots;
