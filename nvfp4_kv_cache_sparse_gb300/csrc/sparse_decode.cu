@@ -918,7 +918,7 @@ bool encode_cache_map(CUtensorMap* map, const uint8_t* cache, int64_t num_slots,
     const cuuint32_t box[2] = {static_cast<cuuint32_t>(record_bytes / 4), 1u};
     const cuuint32_t elem_strides[2] = {1u, 1u};
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint8_t*>(cache), dims, strides, box, elem_strides,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
