@@ -467,6 +467,100 @@ def run_reference(args):
     }
 
 
+# ---------------------------------------------------------------------------------------
+# --sweep: every configuration of the pages' workloads, one JSON line each (not the bench line)
+# ---------------------------------------------------------------------------------------
+
+def _time_calls(fn, iters: int, flush=None) -> float:
+    """Seconds per call. Warm (flush None): `iters` back-to-back calls between two CUDA events,
+    the host running ahead of the device. Cold: `flush` (writes a buffer larger than L2) runs
+    before every call outside its own event pair; the median call is returned."""
+    if flush is None:
+        st, en = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        st.record()
+        for _ in range(iters):
+            fn()
+        en.record()
+        en.synchronize()
+        return st.elapsed_time(en) * 1e-3 / iters
+    times = []
+    for _ in range(iters):
+        flush()
+        st, en = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        st.record()
+        fn()
+        en.record()
+        en.synchronize()
+        times.append(st.elapsed_time(en) * 1e-3)
+    return float(np.median(times))
+
+
+def run_sweep(args):
+    import nvfp4_kv_cache_sparse_gb300 as lib
+    from synth.pool import fill_pool
+    dev = torch.device("cuda", 0)
+    peaks, peak_src = load_peaks()
+    tflops, hbm = float(peaks["bf16_tflops"]), float(peaks["hbm_gbs"])
+    scrub = torch.empty(512 << 20, dtype=torch.uint8, device=dev)   # > L2: written before cold calls
+
+    def flush():
+        scrub.fill_(1)
+
+    iters = max(5, args.sweep_iters)
+    decode_cfgs = [("tiny_b1_h64_topk64_R352", synth.tiny_decode(seed=0)),
+                   ("decode_b32_sq1_h128_topk2048_R352", synth.batch_decode(seed=0)),
+                   ("varlen_b128_sq2_h64_topk2048_R352_sink", synth.varlen_decode(seed=0)),
+                   ("longctx_b64_sq1_h128_topk2048_R432", synth.long_context(seed=0))]
+    for name, w in decode_cfgs:
+        cache = fill_pool(lib.quantize_append, w.num_slots, w.record_bytes, w.pool_seed, dev)
+        q, idx = w.q.to(dev), w.indices.to(dev)
+        sink = None if w.attn_sink is None else w.attn_sink.to(dev)
+        out = torch.empty((w.B, w.s_q, w.h_q, 512), dtype=torch.bfloat16, device=dev)
+        lse = torch.empty((w.B, w.s_q, w.h_q), dtype=torch.float32, device=dev)
+        ws = torch.empty(max(1, lib.workspace_size(w.B, w.s_q, w.h_q, w.topk, w.record_bytes, 0)), dtype=torch.uint8,
+                         device=dev)
+
+        def call():
+            lib.sparse_mla_decode(q, cache, idx, w.sm_scale, attn_sink=sink, out=out, lse=lse, workspace=ws)
+
+        for _ in range(3):
+            call()
+        torch.cuda.synchronize()
+        warm = _time_calls(call, iters)
+        cold = _time_calls(call, iters, flush)
+        flops, bytes_ = roofline_numbers(w)
+        t_roof = max(bytes_ / (hbm * 1e9), flops / (tflops * 1e12))
+        valid = int((w.indices >= 0).sum())
+        print(json.dumps({"sweep": True, "workload": name, "kind": "decode", "query_tokens": w.n_rows,
+                          "us_per_call_warm": warm * 1e6, "us_per_call_cold": cold * 1e6,
+                          "query_tokens_per_s_cold": w.n_rows / cold, "roofline_us": t_roof * 1e6,
+                          "roofline_frac_cold": t_roof / cold, "bound": "tensor" if flops / (tflops * 1e12) >
+                          bytes_ / (hbm * 1e9) else "hbm", "algorithmic_flops": flops, "algorithmic_bytes": bytes_,
+                          "valid_index_fraction": valid / w.indices.numel(), "peaks": peak_src}), flush=True)
+        del cache
+        torch.cuda.empty_cache()
+    # write path (quantize-append of 65,536 tokens into a 262,144-slot pool)
+    ww = synth.write_path(seed=0)
+    cache = torch.full((ww.num_slots, ww.record_bytes), ww.fill_byte, dtype=torch.uint8, device=dev)
+    lat, rope, slots = ww.latent.to(dev), ww.rope.to(dev), ww.slot_mapping.to(dev)
+
+    def append():
+        lib.quantize_append(lat, rope, slots, cache)
+
+    for _ in range(3):
+        append()
+    torch.cuda.synchronize()
+    warm = _time_calls(append, iters)
+    cold = _time_calls(append, iters, flush)
+    bytes_ = ww.T * (512 * 2 + 64 * 2 + 8 + ww.record_bytes)
+    t_roof = bytes_ / (hbm * 1e9)
+    print(json.dumps({"sweep": True, "workload": ww.name, "kind": "quantize_append", "tokens": ww.T,
+                      "us_per_call_warm": warm * 1e6, "us_per_call_cold": cold * 1e6,
+                      "tokens_per_s_cold": ww.T / cold, "achieved_gbs_cold": bytes_ / cold / 1e9,
+                      "roofline_us": t_roof * 1e6, "roofline_frac_cold": t_roof / cold, "bound": "hbm",
+                      "algorithmic_bytes": bytes_, "peaks": peak_src}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -476,7 +570,13 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-rows", type=int, default=4)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sweep", action="store_true",
+                    help="time every workload configuration (decode and write path), one JSON line each")
+    ap.add_argument("--sweep-iters", type=int, default=20)
     args = ap.parse_args()
+    if args.sweep:
+        run_sweep(args)
+        return
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
