@@ -35,6 +35,8 @@ namespace nvfp4mla {
 namespace {
 
 constexpr int kWarpsPerBlock = 8;
+constexpr int kTokensPerRound = 4;
+constexpr int kBlocksPerSm = 4;
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
@@ -73,7 +75,7 @@ __device__ __forceinline__ float round_to_12_bits(float v) {
 }
 
 template <int R>
-__global__ void __launch_bounds__(kWarpsPerBlock * 32)
+__global__ void __launch_bounds__(kWarpsPerBlock * 32, kBlocksPerSm)
 quantize_append_kernel(const uint16_t* __restrict__ latent, int64_t latent_stride, const uint16_t* __restrict__ rope,
                        int64_t rope_stride, const int64_t* __restrict__ slot_mapping, int64_t num_tokens,
                        uint8_t* __restrict__ cache, int64_t num_slots, uint32_t* __restrict__ dev_status) {
@@ -82,58 +84,72 @@ quantize_append_kernel(const uint16_t* __restrict__ latent, int64_t latent_strid
     const int lane = threadIdx.x & 31;
     uint8_t* rec = stage[warp];
 
-    for (int64_t t = static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + warp; t < num_tokens;
-         t += static_cast<int64_t>(gridDim.x) * kWarpsPerBlock) {
-        const int64_t slot = __ldg(slot_mapping + t);
-        if (slot < 0) continue;
-        if (slot >= num_slots) {
-            if (lane == 0 && dev_status != nullptr) atomicOr(dev_status, 0x1u);
-            continue;
-        }
-
-        // ---- NoPE group `lane`: 16 bf16 values = two 16-byte loads
-        const uint4* src = reinterpret_cast<const uint4*>(latent + t * latent_stride) + 2 * lane;
-        const uint4 va = __ldg(src);
-        const uint4 vb = __ldg(src + 1);
-        const uint32_t w[8] = {va.x, va.y, va.z, va.w, vb.x, vb.y, vb.z, vb.w};
-        uint32_t amax_bits = 0;
+    // kTokensPerRound tokens per warp per round: all their loads (slot, 32 latent bytes and 4
+    // RoPE bytes per lane) are issued before any of them is converted, so their memory latencies
+    // overlap.
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kWarpsPerBlock;
+    for (int64_t t0 = static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + warp; t0 < num_tokens;
+         t0 += stride * kTokensPerRound) {
+        int64_t slot[kTokensPerRound];
+        uint4 va[kTokensPerRound], vb[kTokensPerRound];
+        uint32_t rw[kTokensPerRound];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            amax_bits = max(amax_bits, max(w[k] & 0x7FFFu, (w[k] >> 16) & 0x7FFFu));
+        for (int u = 0; u < kTokensPerRound; ++u) {
+            const int64_t t = t0 + u * stride;
+            slot[u] = -1;
+            if (t < num_tokens) {
+                slot[u] = __ldg(slot_mapping + t);
+                const uint4* src = reinterpret_cast<const uint4*>(latent + t * latent_stride) + 2 * lane;
+                va[u] = __ldg(src);
+                vb[u] = __ldg(src + 1);
+                rw[u] = __ldg(reinterpret_cast<const uint32_t*>(rope + t * rope_stride) + lane);
+            }
         }
-        const float amax = __uint_as_float(amax_bits << 16);
-        const uint32_t sbyte = e4m3x2_rn_sat(0.0f, __fdiv_rn(amax, 6.0f)) & 0xFFu;
-        const float inv_s = sbyte ? __frcp_rn(e4m3_code_value(sbyte)) : 0.0f;
-
-        uint32_t packed[2] = {0u, 0u};
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const float q0 = round_to_12_bits(fabsf(bf16_lo(w[k])) * inv_s);
-            const float q1 = round_to_12_bits(fabsf(bf16_hi(w[k])) * inv_s);
-            uint32_t byte = e2m1x2_rn_sat(q1, q0);                    // even element -> low nibble
-            byte |= ((w[k] >> 12) & 0x8u) | ((w[k] >> 24) & 0x80u);   // signs of both elements
-            packed[k >> 2] |= byte << (8 * (k & 3));
-        }
-        *reinterpret_cast<uint2*>(rec + 8 * lane) = make_uint2(packed[0], packed[1]);
+        for (int u = 0; u < kTokensPerRound; ++u) {
+            if (slot[u] < 0) continue;                       // padding token (or past the end)
+            if (slot[u] >= num_slots) {
+                if (lane == 0 && dev_status != nullptr) atomicOr(dev_status, 0x1u);
+                continue;
+            }
+            // ---- NoPE group `lane`: 16 bf16 values
+            const uint32_t w[8] = {va[u].x, va[u].y, va[u].z, va[u].w, vb[u].x, vb[u].y, vb[u].z, vb[u].w};
+            uint32_t amax_bits = 0;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) amax_bits = max(amax_bits, max(w[k] & 0x7FFFu, (w[k] >> 16) & 0x7FFFu));
+            const float amax = __uint_as_float(amax_bits << 16);
+            const uint32_t sbyte = e4m3x2_rn_sat(0.0f, __fdiv_rn(amax, 6.0f)) & 0xFFu;
+            const float inv_s = sbyte ? __frcp_rn(e4m3_code_value(sbyte)) : 0.0f;
 
-        // ---- RoPE: lane owns elements 2*lane and 2*lane+1
-        const uint32_t rw = __ldg(reinterpret_cast<const uint32_t*>(rope + t * rope_stride) + lane);
-        if constexpr (R == 352) {
-            rec[320 + 8 * (lane & 3) + (lane >> 2)] = static_cast<uint8_t>(sbyte);
-            uint32_t c = e4m3x2_rn_sat(fabsf(bf16_hi(rw)), fabsf(bf16_lo(rw)));
-            c |= ((rw >> 8) & 0x80u) | ((rw >> 16) & 0x8000u);
-            *reinterpret_cast<uint16_t*>(rec + 256 + 2 * lane) = static_cast<uint16_t>(c);
-        } else {
-            rec[256 + lane] = static_cast<uint8_t>(sbyte);
-            *reinterpret_cast<uint32_t*>(rec + 304 + 4 * lane) = rw;
-            if (lane < 4) *reinterpret_cast<uint32_t*>(rec + 288 + 4 * lane) = 0u;
+            uint32_t packed[2] = {0u, 0u};
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const float q0 = round_to_12_bits(fabsf(bf16_lo(w[k])) * inv_s);
+                const float q1 = round_to_12_bits(fabsf(bf16_hi(w[k])) * inv_s);
+                uint32_t byte = e2m1x2_rn_sat(q1, q0);                    // even element -> low nibble
+                byte |= ((w[k] >> 12) & 0x8u) | ((w[k] >> 24) & 0x80u);   // signs of both elements
+                packed[k >> 2] |= byte << (8 * (k & 3));
+            }
+            *reinterpret_cast<uint2*>(rec + 8 * lane) = make_uint2(packed[0], packed[1]);
+
+            // ---- RoPE: lane owns elements 2*lane and 2*lane+1
+            if constexpr (R == 352) {
+                rec[320 + 8 * (lane & 3) + (lane >> 2)] = static_cast<uint8_t>(sbyte);
+                uint32_t c = e4m3x2_rn_sat(fabsf(bf16_hi(rw[u])), fabsf(bf16_lo(rw[u])));
+                c |= ((rw[u] >> 8) & 0x80u) | ((rw[u] >> 16) & 0x8000u);
+                *reinterpret_cast<uint16_t*>(rec + 256 + 2 * lane) = static_cast<uint16_t>(c);
+            } else {
+                rec[256 + lane] = static_cast<uint8_t>(sbyte);
+                *reinterpret_cast<uint32_t*>(rec + 304 + 4 * lane) = rw[u];
+                if (lane < 4) *reinterpret_cast<uint32_t*>(rec + 288 + 4 * lane) = 0u;
+            }
+            __syncwarp();
+            if (lane < R / 16) {
+                const uint4 v = reinterpret_cast<const uint4*>(rec)[lane];
+                reinterpret_cast<uint4*>(cache + slot[u] * R)[lane] = v;
+            }
+            __syncwarp();
         }
-        __syncwarp();
-        if (lane < R / 16) {
-            const uint4 v = reinterpret_cast<const uint4*>(rec)[lane];
-            reinterpret_cast<uint4*>(cache + slot * R)[lane] = v;
-        }
-        __syncwarp();
     }
 }
 
@@ -144,7 +160,7 @@ cudaError_t launch_quantize_append(const void* kv_latent, int64_t latent_row_str
                                    uint8_t* cache, int64_t num_slots, int record_bytes, uint32_t* dev_status,
                                    int sm_count, cudaStream_t stream) {
     const int64_t want = (num_tokens + kWarpsPerBlock - 1) / kWarpsPerBlock;
-    const int64_t cap = static_cast<int64_t>(sm_count) * 8;   // 8 blocks of 256 threads per SM
+    const int64_t cap = static_cast<int64_t>(sm_count) * kBlocksPerSm;   // one wave of resident blocks
     const int grid = static_cast<int>(want < cap ? want : cap);
     const dim3 block(kWarpsPerBlock * 32);
     const auto* lat = static_cast<const uint16_t*>(kv_latent);
