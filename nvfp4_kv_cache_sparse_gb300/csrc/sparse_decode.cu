@@ -12,18 +12,24 @@
 // Work split: a cluster of two CTAs per (query row, top-k split), with different roles.
 // With 128 heads, the fp32 accumulator O [128 x 512] fills all 512 TMEM columns of an SM, so
 // QK^T and PV run on different SMs and only the bf16 P tile travels between them:
-//   CTA 0 (QK): gathers whole records, dequantizes K tiles (576 dims), keeps Q [128 x 576]
-//     in TMEM as the MMA A operand, computes S = Q K^T, runs the online softmax, and sends
+//   CTA 0 (QK): keeps Q [128 x 576] in TMEM as the MMA A operand (loaded by nine TMA boxes),
+//     dequantizes K tiles (576 dims), computes S = Q K^T, runs the online softmax, and sends
 //     each row's P (bf16) and rescale factor to CTA 1 with st.async (DSMEM, one way:
 //     132 B per head per 64 keys).
-//   CTA 1 (PV): gathers the NoPE half of the same records, dequantizes V tiles (512 dims),
-//     keeps O in TMEM and computes O += P V with P read from shared memory; its MMA commit
-//     multicasts back to CTA 0 to release the P slot. At the end CTA 0 sends each row's
-//     running max and sum, and CTA 1 normalizes and writes `out` (CTA 0 writes `lse`).
-// Warp roles (448 threads):
-//   CTA 0: warps 0-3 softmax (thread r = head r = TMEM lane r), 4-11 gather/dequant,
-//          12-13 QK issuers (even / odd tiles; one elected lane each).
-//   CTA 1: warps 0-3 rescale/epilogue (thread r = TMEM lane r), 4-11 gather/dequant, 12 PV issuer.
+//   CTA 1 (PV): dequantizes V tiles (the 512 NoPE dims of the same records), keeps O in
+//     TMEM and computes O += P V with P read from shared memory; its MMA commit multicasts
+//     back to CTA 0 to release the P slot. At the end CTA 0 sends each row's running max and
+//     sum, and CTA 1 normalizes, writes `out` (or the split's partial) and `lse`.
+// Warp roles (kThreads = 896 threads, 28 warps):
+//   both:  warps 8-23 convert (8 threads per key of a 64-key tile), warps 26-27 gather
+//          records with TMA tile::gather4 into a ring of raw tiles (CTA 0: three for 352-B
+//          records, two for 432-B; CTA 1: two) and publish the used-key bits of each
+//          tile; warp 24 owns tensor memory.
+//   CTA 0: warps 0-7 softmax (warp w: TMEM lanes 32 (w & 3).., score columns 32 (w >> 2)..+32;
+//          the two column halves exchange tile maxima), warps 24-25 QK issuers (even / odd
+//          tiles; one elected lane each).
+//   CTA 1: warps 0-3 rescale O and stage the output (thread r = TMEM lane r), warp 24 PV
+//          issuer; the converter warps copy the staged output out.
 // Tiles are 64 keys; every K/V tile is written in a 128B-swizzled layout that is the K-major
 // B operand of QK (CTA 0) or the MN-major B operand of PV (CTA 1).
 //
