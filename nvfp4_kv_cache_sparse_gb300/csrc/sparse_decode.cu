@@ -633,31 +633,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) sparse_
                     if (m_ref != -INFINITY) alpha = ex2_approx(m_ref - tile_max);
                     m_ref = tile_max;
                 }
-                uint32_t p[16];
-                if (m_ref != -INFINITY) {
-                    const uint64_t mul2 = f32x2_pack(zs, zs);
-                    const uint64_t neg_m2 = f32x2_pack(-m_ref, -m_ref);
-                    uint64_t la = f32x2_pack(0.0f, 0.0f), lb = la;
-#pragma unroll
-                    for (int j = 0; j < 32; j += 4) {
-                        const float2 z0 = f32x2_unpack(
-                            f32x2_fma(f32x2_pack(__uint_as_float(s[j]), __uint_as_float(s[j + 1])), mul2, neg_m2));
-                        const float2 z1 = f32x2_unpack(
-                            f32x2_fma(f32x2_pack(__uint_as_float(s[j + 2]), __uint_as_float(s[j + 3])), mul2, neg_m2));
-                        const float p0 = ex2_approx(z0.x), p1 = ex2_approx(z0.y);
-                        const float p2 = ex2_approx(z1.x), p3 = ex2_approx(z1.y);
-                        la = f32x2_add(la, f32x2_pack(p0, p1));
-                        lb = f32x2_add(lb, f32x2_pack(p2, p3));
-                        p[j / 2] = pack_bf16x2(p0, p1);
-                        p[j / 2 + 1] = pack_bf16x2(p2, p3);
-                    }
-                    const float2 sa = f32x2_unpack(la), sb = f32x2_unpack(lb);
-                    l = l * alpha + ((sa.x + sa.y) + (sb.x + sb.y));
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) p[j] = 0u;
-                }
-                // ---- this half of P row h (and alpha) -> CTA 1's slot (i % kPStages), once its PV released it
+                // ---- this half of P row h (and alpha) -> CTA 1's slot (i % kPStages), once its PV
+                // released it; each 16-byte chunk is sent as soon as its eight exponentials exist
                 const int ps = i % kPStages;
                 if (i >= kPStages) {
                     ok = wait_warp(ctl, &ctl->pempty[ps], ((i / kPStages) - 1) & 1, a.status);
@@ -665,10 +642,35 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) sparse_
                 }
                 const uint32_t dst = peer_p + ps * kPBytes;
                 const uint32_t bar = peer_pfull0 + 8 * ps;
+                if (m_ref != -INFINITY) {
+                    const uint64_t mul2 = f32x2_pack(zs, zs);
+                    const uint64_t neg_m2 = f32x2_pack(-m_ref, -m_ref);
+                    uint64_t la = f32x2_pack(0.0f, 0.0f), lb = la;
 #pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    st_async_u4(dst + (((4 * half + c) ^ (h & 7)) << 4),
-                                make_uint4(p[4 * c], p[4 * c + 1], p[4 * c + 2], p[4 * c + 3]), bar);
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t p[4];
+#pragma unroll
+                        for (int j = 8 * c; j < 8 * c + 8; j += 4) {
+                            const float2 z0 = f32x2_unpack(
+                                f32x2_fma(f32x2_pack(__uint_as_float(s[j]), __uint_as_float(s[j + 1])), mul2, neg_m2));
+                            const float2 z1 = f32x2_unpack(
+                                f32x2_fma(f32x2_pack(__uint_as_float(s[j + 2]), __uint_as_float(s[j + 3])), mul2, neg_m2));
+                            const float p0 = ex2_approx(z0.x), p1 = ex2_approx(z0.y);
+                            const float p2 = ex2_approx(z1.x), p3 = ex2_approx(z1.y);
+                            la = f32x2_add(la, f32x2_pack(p0, p1));
+                            lb = f32x2_add(lb, f32x2_pack(p2, p3));
+                            p[(j & 7) / 2] = pack_bf16x2(p0, p1);
+                            p[(j & 7) / 2 + 1] = pack_bf16x2(p2, p3);
+                        }
+                        st_async_u4(dst + (((4 * half + c) ^ (h & 7)) << 4), make_uint4(p[0], p[1], p[2], p[3]), bar);
+                    }
+                    const float2 sa = f32x2_unpack(la), sb = f32x2_unpack(lb);
+                    l = l * alpha + ((sa.x + sa.y) + (sb.x + sb.y));
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        st_async_u4(dst + (((4 * half + c) ^ (h & 7)) << 4), make_uint4(0u, 0u, 0u, 0u), bar);
+                }
                 if (half == 0) st_async_f32(peer_alpha + ps * kHeadsM * 4, alpha, bar);
             }
             // ---- running max and the merged row sum to CTA 1, which writes out and lse
