@@ -148,6 +148,12 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N, bo
            ((N >> 3) << 17) | ((M >> 4) << 24);
 }
 
+// Same with A and B in f16 (a/b type fields 0).
+__host__ __device__ constexpr uint32_t idesc_f16_f32(uint32_t M, uint32_t N, bool a_mn_major, bool b_mn_major) {
+    return (1u << 4) | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) | ((N >> 3) << 17) |
+           ((M >> 4) << 24);
+}
+
 // Shared-memory matrix descriptor for a 128-byte-swizzled operand.
 //   [0,14) start address >> 4   [16,30) leading byte offset >> 4   [32,46) stride byte offset >> 4
 //   [46,48) version (1 on sm_100 family)   [49,52) base offset (0: atoms 1024-byte aligned)

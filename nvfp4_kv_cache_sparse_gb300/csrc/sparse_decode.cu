@@ -171,6 +171,12 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&b);
 }
 
+// P entries lie in [0, 2^8] (lazy reference max), so f16 holds them with 11 significant bits.
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    const __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&v);
+}
+
 // Two e2m1 codes (one byte: low nibble = even element) times a scale -> bf16x2 (exact).
 __device__ __forceinline__ uint32_t dq_e2m1x2(uint32_t byte, __half2 scale2) {
     uint32_t h;
@@ -184,6 +190,21 @@ __device__ __forceinline__ uint32_t dq_e2m1x2(uint32_t byte, __half2 scale2) {
     __half2 v = __hmul2(*reinterpret_cast<__half2*>(&h), scale2);
     const float2 f = __half22float2(v);
     return pack_bf16x2(f.x, f.y);
+}
+
+// Two e2m1 codes times a scale -> f16x2 (exact: the products need at most 5 significant bits and
+// lie in [2^-10, 2688], inside the f16 normal range).
+__device__ __forceinline__ uint32_t dq_e2m1x2_f16(uint32_t byte, __half2 scale2) {
+    uint32_t h;
+    asm("{\n"
+        "  .reg .b8 t;\n"
+        "  cvt.u8.u32 t, %1;\n"
+        "  cvt.rn.f16x2.e2m1x2 %0, t;\n"
+        "}\n"
+        : "=r"(h)
+        : "r"(byte));
+    const __half2 v = __hmul2(*reinterpret_cast<__half2*>(&h), scale2);
+    return *reinterpret_cast<const uint32_t*>(&v);
 }
 
 // Two e4m3 codes (low byte = even element) -> bf16x2 (exact).
@@ -204,16 +225,26 @@ __device__ __forceinline__ __half2 scale_half2(uint32_t sbyte) {
 }
 
 // 16 e2m1 values (8 bytes) of one 16-wide block times its scale -> 2 x 16 bytes of bf16.
+// kF16: f16 output (the PV operand), else bf16 (the QK operand).
+template <bool kF16>
+__device__ __forceinline__ uint32_t dq_pair(uint32_t byte, __half2 scale2) {
+    if constexpr (kF16)
+        return dq_e2m1x2_f16(byte, scale2);
+    else
+        return dq_e2m1x2(byte, scale2);
+}
+
+template <bool kF16>
 __device__ __forceinline__ void dq_block(uint2 codes, uint32_t sbyte, uint4& lo, uint4& hi) {
     const __half2 s2 = scale_half2(sbyte);
-    lo.x = dq_e2m1x2(codes.x & 0xFFu, s2);
-    lo.y = dq_e2m1x2((codes.x >> 8) & 0xFFu, s2);
-    lo.z = dq_e2m1x2((codes.x >> 16) & 0xFFu, s2);
-    lo.w = dq_e2m1x2(codes.x >> 24, s2);
-    hi.x = dq_e2m1x2(codes.y & 0xFFu, s2);
-    hi.y = dq_e2m1x2((codes.y >> 8) & 0xFFu, s2);
-    hi.z = dq_e2m1x2((codes.y >> 16) & 0xFFu, s2);
-    hi.w = dq_e2m1x2(codes.y >> 24, s2);
+    lo.x = dq_pair<kF16>(codes.x & 0xFFu, s2);
+    lo.y = dq_pair<kF16>((codes.x >> 8) & 0xFFu, s2);
+    lo.z = dq_pair<kF16>((codes.x >> 16) & 0xFFu, s2);
+    lo.w = dq_pair<kF16>(codes.x >> 24, s2);
+    hi.x = dq_pair<kF16>(codes.y & 0xFFu, s2);
+    hi.y = dq_pair<kF16>((codes.y >> 8) & 0xFFu, s2);
+    hi.z = dq_pair<kF16>((codes.y >> 16) & 0xFFu, s2);
+    hi.w = dq_pair<kF16>(codes.y >> 24, s2);
 }
 
 __device__ __forceinline__ void set_abort(SmemCtl* ctl, uint32_t* status) {
@@ -277,7 +308,7 @@ __device__ __forceinline__ void convert_part(uint32_t rec, bool valid, uint32_t 
         for (int j = 0; j < 4; ++j) {
             const int c = 4 * hi + j;
             uint4 lo, hv;
-            dq_block(codes[j], (sw >> (8 * j)) & 0xFFu, lo, hv);
+            dq_block<!kRope>(codes[j], (sw >> (8 * j)) & 0xFFu, lo, hv);
             sts_u128(tile + c * kBlkBytes + swz(key, 2 * q), lo);
             sts_u128(tile + c * kBlkBytes + swz(key, 2 * q + 1), hv);
         }
@@ -659,8 +690,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) sparse_
                             const float p2 = ex2_approx(z1.x), p3 = ex2_approx(z1.y);
                             la = f32x2_add(la, f32x2_pack(p0, p1));
                             lb = f32x2_add(lb, f32x2_pack(p2, p3));
-                            p[(j & 7) / 2] = pack_bf16x2(p0, p1);
-                            p[(j & 7) / 2 + 1] = pack_bf16x2(p2, p3);
+                            p[(j & 7) / 2] = pack_f16x2(p0, p1);
+                            p[(j & 7) / 2 + 1] = pack_f16x2(p2, p3);
                         }
                         st_async_u4(dst + (((4 * half + c) ^ (h & 7)) << 4), make_uint4(p[0], p[1], p[2], p[3]), bar);
                     }
@@ -791,7 +822,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) sparse_
         } else if (warp == kWarpMma) {
             // ============ CTA 1, warp 24: PV issuer (warps 4-7 and 25 idle) ============
             cluster_wait();          // CTA 0's pempty barriers exist before the first multicast commit
-            const uint32_t idesc_pv = idesc_bf16_f32(kHeadsM, 256, false, true);
+            const uint32_t idesc_pv = idesc_f16_f32(kHeadsM, 256, false, true);
             const uint64_t pdesc0 = sdesc_sw128(smem_addr(smem + kOffP), 16, 1024);
             const uint64_t vdesc0 = sdesc_sw128(smem_addr(smem + kOffV), kBlkBytes, 1024);
             const bool leader = elect_one_in_warp();
