@@ -6,16 +6,17 @@
 //     z_j = sm_scale * q[t,h,:] . K_j          (K_j: 576 dequantized values of record j)
 //     out = sum_j e^{z_j} V_j / (sum_j e^{z_j} + e^{sink_h}),   V_j = K_j[0:512]
 //     lse = ln sum_j e^{z_j}
-// Keys are dequantized to bf16 in shared memory (exact: e2m1 x e4m3 has <= 5 significant
-// bits); both contractions run as tcgen05 bf16 MMAs with fp32 accumulation in tensor memory.
+// Keys are dequantized in shared memory, exactly (e2m1 x e4m3 has <= 5 significant bits): to
+// bf16 for QK^T (q is bf16) and to f16 for PV (P in f16 keeps 11 significant bits); both
+// contractions run as tcgen05 16-bit MMAs with fp32 accumulation in tensor memory.
 //
 // Work split: a cluster of two CTAs per (query row, top-k split), with different roles.
 // With 128 heads, the fp32 accumulator O [128 x 512] fills all 512 TMEM columns of an SM, so
-// QK^T and PV run on different SMs and only the bf16 P tile travels between them:
+// QK^T and PV run on different SMs and only the 16-bit P tile travels between them:
 //   CTA 0 (QK): keeps Q [128 x 576] in TMEM as the MMA A operand (loaded by nine TMA boxes),
 //     dequantizes K tiles (576 dims), computes S = Q K^T, runs the online softmax, and sends
-//     each row's P (bf16) and rescale factor to CTA 1 with st.async (DSMEM, one way:
-//     132 B per head per 64 keys).
+//     each row's P (f16) and rescale factor to CTA 1 with st.async (DSMEM, one way:
+//     132 B per head per 64 keys; each store instruction covers 8 rows x 64 B).
 //   CTA 1 (PV): dequantizes V tiles (the 512 NoPE dims of the same records), keeps O in
 //     TMEM and computes O += P V with P read from shared memory; its MMA commit multicasts
 //     back to CTA 0 to release the P slot. At the end CTA 0 sends each row's running max and
@@ -58,7 +59,7 @@ constexpr int kKStages = 2;                        // CTA 0: K tiles of 9 blocks
 constexpr int kKTileBytes = 9 * kBlkBytes;         // 72 KB
 constexpr int kVStages = 2;                        // CTA 1: V tiles of 8 blocks
 constexpr int kVTileBytes = 8 * kBlkBytes;         // 64 KB
-constexpr int kPStages = 2;                        // CTA 1: P tiles [128 heads x 64 keys] bf16
+constexpr int kPStages = 2;                        // CTA 1: P tiles [128 heads x 64 keys] f16
 constexpr int kPBytes = kHeadsM * 128;             // 16 KB
 constexpr int kMaskSlots = 16;
 // Raw-record ring, filled by TMA tile::gather4 (four whole records per instruction, each group of
@@ -418,6 +419,35 @@ __device__ __forceinline__ void convert_tiles(const KernelArgs& a, SmemCtl* ctl,
     }
 }
 
+// One word of a chunk swap with lane ^ xor_mask: the lane gives `a` and takes the partner's
+// word into `a` when give_a, else gives and takes `b`.
+__device__ __forceinline__ void swap_word(uint32_t& a, uint32_t& b, bool give_a, int xor_mask) {
+    const uint32_t r = __shfl_xor_sync(0xffffffffu, give_a ? a : b, xor_mask);
+    a = give_a ? r : a;
+    b = give_a ? b : r;
+}
+
+// In each group of four lanes (k = lane & 3) holding chunks c[0..3] of their own rows, leaves
+// chunk k of lane (4a + j)'s row in c[j]: two butterfly exchanges of half the chunks each.
+__device__ __forceinline__ void transpose4_chunks(uint4 (&c)[4], int lane) {
+    const bool up = (lane & 2) != 0;   // lanes k, k ^ 2 swap the chunks whose bit 1 differs from k's
+#pragma unroll
+    for (int m = 0; m < 2; ++m) {
+        swap_word(c[m].x, c[m + 2].x, up, 2);
+        swap_word(c[m].y, c[m + 2].y, up, 2);
+        swap_word(c[m].z, c[m + 2].z, up, 2);
+        swap_word(c[m].w, c[m + 2].w, up, 2);
+    }
+    const bool odd = (lane & 1) != 0;  // lanes k, k ^ 1 swap the chunks whose bit 0 differs from k's
+#pragma unroll
+    for (int m = 0; m < 2; ++m) {
+        swap_word(c[2 * m].x, c[2 * m + 1].x, odd, 1);
+        swap_word(c[2 * m].y, c[2 * m + 1].y, odd, 1);
+        swap_word(c[2 * m].z, c[2 * m + 1].z, odd, 1);
+        swap_word(c[2 * m].w, c[2 * m + 1].w, odd, 1);
+    }
+}
+
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t threads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
@@ -602,12 +632,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) sparse_
                 mbar_arrive(&ctl->qready);
             }
             cluster_wait();
-            // row h of CTA 1's P slot 0 (128B-swizzled K-major rows; chunk c at (c ^ (h & 7)) * 16)
-            const uint32_t peer_p = mapa_shared(smem_addr(smem + kOffP) + (h >> 3) * 1024 + (h & 7) * 128, 1);
+            // 8-row atom of row h in CTA 1's P slot 0 (128B-swizzled K-major rows; chunk c of row r
+            // of the atom at r * 128 + (c ^ r) * 16)
+            const uint32_t peer_p_atom = mapa_shared(smem_addr(smem + kOffP) + (h >> 3) * 1024, 1);
             const uint32_t peer_alpha = mapa_shared(smem_addr(smem + kOffAlpha) + 4 * h, 1);
-            const uint32_t peer_fin = mapa_shared(smem_addr(smem + kOffFin) + 8 * h, 1);
             const uint32_t peer_pfull0 = mapa_shared(smem_addr(&ctl->pfull[0]), 1);
-            const uint32_t peer_finbar = mapa_shared(smem_addr(&ctl->fin), 1);
             float* xmax = reinterpret_cast<float*>(smem + SmemSize<R>::xchg0);   // [parity][half][128]
             float* xsum = xmax + 4 * kHeadsM;                                      // [128]
             float m_ref = -INFINITY;   // reference max, log2 units of scaled logits (same in both halves)
@@ -664,15 +693,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) sparse_
                     if (m_ref != -INFINITY) alpha = ex2_approx(m_ref - tile_max);
                     m_ref = tile_max;
                 }
-                // ---- this half of P row h (and alpha) -> CTA 1's slot (i % kPStages), once its PV
-                // released it; each 16-byte chunk is sent as soon as its eight exponentials exist
-                const int ps = i % kPStages;
-                if (i >= kPStages) {
-                    ok = wait_warp(ctl, &ctl->pempty[ps], ((i / kPStages) - 1) & 1, a.status);
-                    if (!ok) break;
-                }
-                const uint32_t dst = peer_p + ps * kPBytes;
-                const uint32_t bar = peer_pfull0 + 8 * ps;
+                uint4 pc[4];   // this half of P row h: chunk j = keys 32 half + 8j .. +7 (f16)
                 if (m_ref != -INFINITY) {
                     const uint64_t mul2 = f32x2_pack(zs, zs);
                     const uint64_t neg_m2 = f32x2_pack(-m_ref, -m_ref);
@@ -693,14 +714,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) sparse_
                             p[(j & 7) / 2] = pack_f16x2(p0, p1);
                             p[(j & 7) / 2 + 1] = pack_f16x2(p2, p3);
                         }
-                        st_async_u4(dst + (((4 * half + c) ^ (h & 7)) << 4), make_uint4(p[0], p[1], p[2], p[3]), bar);
+                        pc[c] = make_uint4(p[0], p[1], p[2], p[3]);
                     }
                     const float2 sa = f32x2_unpack(la), sb = f32x2_unpack(lb);
                     l = l * alpha + ((sa.x + sa.y) + (sb.x + sb.y));
                 } else {
 #pragma unroll
-                    for (int c = 0; c < 4; ++c)
-                        st_async_u4(dst + (((4 * half + c) ^ (h & 7)) << 4), make_uint4(0u, 0u, 0u, 0u), bar);
+                    for (int c = 0; c < 4; ++c) pc[c] = make_uint4(0u, 0u, 0u, 0u);
+                }
+                // ---- 4 x 4 transpose of 16-byte chunks inside each group of four lanes: lane 4a + k
+                // ends up with chunk k of the rows of lanes 4a .. 4a + 3, so that every store below
+                // writes 8 rows x 64 contiguous bytes (DSMEM moves 64-byte pieces at twice the rate
+                // of 16-byte ones)
+                transpose4_chunks(pc, lane);
+                // ---- -> CTA 1's slot (i % kPStages), once its PV released it
+                const int ps = i % kPStages;
+                if (i >= kPStages) {
+                    ok = wait_warp(ctl, &ctl->pempty[ps], ((i / kPStages) - 1) & 1, a.status);
+                    if (!ok) break;
+                }
+                const uint32_t bar = peer_pfull0 + 8 * ps;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const int r = (h & 4) + c;    // row (h & ~3) + c, within its 8-row atom
+                    st_async_u4(peer_p_atom + ps * kPBytes + r * 128 + (((4 * half + (lane & 3)) ^ r) << 4), pc[c], bar);
                 }
                 if (half == 0) st_async_f32(peer_alpha + ps * kHeadsM * 4, alpha, bar);
             }
@@ -709,7 +746,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) sparse_
                 xsum[h] = l;
                 mbar_arrive(&ctl->lbar);
             } else if (ok && wait_warp(ctl, &ctl->lbar, 0, a.status)) {
-                st_async_v2(peer_fin, m_ref, l + xsum[h], peer_finbar);
+                st_async_v2(mapa_shared(smem_addr(smem + kOffFin) + 8 * h, 1), m_ref, l + xsum[h],
+                            mapa_shared(smem_addr(&ctl->fin), 1));
             }
         } else if (converter) {
             // ============ CTA 0, warps 8-23: dequant of whole records (K tiles) ============

@@ -1,7 +1,7 @@
 """Sparse MLA decode on the GPU against the CPU oracle.
 
 Tolerances: |out - ref| <= 1e-2 + 1e-2 |ref| element by element and |lse - ref| <= 1e-3
-(-inf must match exactly). The dequantized keys are exact, so the bf16 rounding of P, the
+(-inf must match exactly). The dequantized keys are exact, so the 16-bit rounding of P, the
 fp32 accumulation order in the tensor core and the final bf16 rounding of `out` are the only
 differences from the fp64 oracle.
 
@@ -116,6 +116,26 @@ def test_edge_rows_empty_single_duplicate_out_of_range():
         assert_close(out, lse, ref_out, ref_lse)
         o = out.float().cpu().numpy()
         assert np.all(o[0] == 0) and np.all(np.isneginf(lse[0].cpu().numpy()))
+
+
+@pytest.mark.parametrize("e", [-30, -12, 0, 20])
+def test_query_magnitudes_outside_the_f16_range(e):
+    """Queries of magnitude 2^e with sm_scale 2^-e / 24 give ordinary logits: q enters the
+    tensor core unchanged at any magnitude (tiny rows, rows above the f16 maximum, a zero head,
+    and a head whose odd dims are 2^-20 of the rest)."""
+    rng = np.random.default_rng(40 + e)
+    B, H, topk, n_slots = 2, 128, 150, 400
+    q = rng.standard_normal((B, 1, H, 576)).astype(np.float32)
+    q[:, :, 5] = 0.0
+    q[:, :, 7, 1::2] *= 2.0 ** -20
+    q *= 2.0 ** e
+    idx = np.stack([rng.choice(n_slots, size=topk, replace=False) for _ in range(B)]).reshape(B, 1, topk)
+    idx = idx.astype(np.int32)
+    for splits in (1, 2):
+        out, lse, ref_out, ref_lse, st = run_small(q, idx, 352, n_slots, 13, 2.0 ** -e / 24.0, None, splits)
+        assert st == 0
+        assert_close(out, lse, ref_out, ref_lse)
+        assert np.allclose(lse.cpu().numpy()[:, :, 5], math.log(topk), atol=1e-4)
 
 
 def test_zero_query_is_mean_of_values_and_splits_agree():
