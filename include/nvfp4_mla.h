@@ -88,8 +88,8 @@ NVFP4_MLA_API int nvfp4_mla_quantize_append(const void* kv_latent, int64_t laten
  *   computed in parallel and merged by a second kernel (launched as a programmatic dependent
  *   of the first on the same stream); 0 lets the library choose from the problem size and the
  *   SM count of the current device (then this call reads the device attribute). The workspace
- *   holds fp32 partial outputs and log-sum-exps of every part; it is 0 bytes when a single
- *   part is used.
+ *   holds each part's normalized partial output (f16, [rows, parts, h_q, 512]) and fp32
+ *   log-sum-exp; it is 0 bytes when a single part is used.
  * Returns NVFP4_MLA_OK and sets *bytes, or an error code for an invalid problem.
  */
 NVFP4_MLA_API int nvfp4_sparse_mla_decode_workspace_size(int32_t batch, int32_t s_q, int32_t h_q,
@@ -118,8 +118,10 @@ NVFP4_MLA_API int nvfp4_sparse_mla_decode_workspace_size(int32_t batch, int32_t 
  *                arguments, 256-byte aligned; may be NULL when that size is 0. Its contents
  *                need no initialization.
  *   dev_status   nullable device uint32 (see NVFP4_MLA_DEV_*).
- * Precision: dequantized keys are exact in bf16; the two contractions run on tcgen05 bf16
- * MMAs with fp32 accumulation; softmax in fp32; `out` is rounded to bf16 once.
+ * Precision: dequantized keys are exact (bf16 for QK^T, f16 for PV); the two contractions
+ * run on tcgen05 16-bit MMAs with fp32 accumulation (P enters PV as f16); softmax in fp32;
+ * `out` is rounded to bf16 once, after the parts' f16 partial outputs (relative error
+ * <= 2^-11 each) are merged in fp32 when the top-k list is split.
  */
 NVFP4_MLA_API int nvfp4_sparse_mla_decode(const void* q, const uint8_t* cache, int64_t num_slots,
                                           int32_t record_bytes, const int32_t* indices,

@@ -66,12 +66,12 @@ int auto_splits(int64_t rows, int32_t topk, int sm_count) {
 
 size_t round256(size_t n) { return (n + 255) & ~size_t(255); }
 
-// Workspace (splits > 1): fp32 partial outputs [rows, splits, h_q, 512], then the partial
+// Workspace (splits > 1): f16 partial outputs [rows, splits, h_q, 512], then the fp32 partial
 // log2-sum-exps [rows, splits, h_q].
 size_t workspace_for(int64_t rows, int32_t h_q, int splits) {
     if (splits <= 1) return 0;
     const size_t n = static_cast<size_t>(rows) * splits * h_q;
-    return n * 512 * sizeof(float) + round256(n * sizeof(float));
+    return n * 512 * sizeof(uint16_t) + round256(n * sizeof(float));
 }
 
 int check_decode_shape(int32_t batch, int32_t s_q, int32_t h_q, int32_t topk, int32_t record_bytes,
@@ -161,8 +161,8 @@ NVFP4_MLA_API int nvfp4_sparse_mla_decode(const void* q, const uint8_t* cache, i
     d.splits = splits;
     const size_t n_part = static_cast<size_t>(rows) * splits * h_q;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
-    d.part_out = need ? reinterpret_cast<float*>(ws) : nullptr;
-    d.part_lse = need ? reinterpret_cast<float*>(ws + n_part * 512 * sizeof(float)) : nullptr;
+    d.part_out = need ? reinterpret_cast<uint16_t*>(ws) : nullptr;
+    d.part_lse = need ? reinterpret_cast<float*>(ws + n_part * 512 * sizeof(uint16_t)) : nullptr;
     d.dev_status = dev_status;
     const cudaError_t e = nvfp4mla::launch_sparse_decode(d, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? NVFP4_MLA_OK : NVFP4_MLA_ERR_CUDA;

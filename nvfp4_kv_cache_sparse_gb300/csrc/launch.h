@@ -27,7 +27,7 @@ struct DecodeArgs {
     void* out;                 // bf16 [rows, h_q, 512]
     float* lse;                // [rows, h_q]
     int splits;
-    float* part_out;           // fp32 [rows, splits, h_q, 512] when splits > 1
+    uint16_t* part_out;        // f16 [rows, splits, h_q, 512] when splits > 1 (O / l of each split)
     float* part_lse;           // fp32 [rows, splits, h_q], log2 domain
     uint32_t* dev_status;
 };

@@ -157,7 +157,7 @@ struct KernelArgs {
     const float* sink;
     __nv_bfloat16* out;
     float* lse;
-    float* part_out;
+    uint16_t* part_out;          // f16 partial outputs [rows, splits, h_q, 512]
     float* part_lse;
     uint32_t* status;
 };
@@ -453,8 +453,8 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t threads) {
 }
 
 // Output of CTA 1: O * factor for the row's 128 x 512 block goes out (bf16 `out` when there is
-// one split, fp32 partial otherwise) through shared memory, so every warp store covers whole
-// 128-byte lines. Four quarters of 128 columns are staged in the two V stages alternately (row h
+// one split, the split's f16 partial otherwise) through shared memory, so every warp store
+// covers whole 128-byte lines. Four quarters of 128 columns are staged in the two V stages alternately (row h
 // at h * 512, 16-byte chunk k at slot k ^ (h & 7)) by warps 0-3 (thread h = TMEM lane h) and
 // copied out by the converter warps (one row per warp instruction), so staging of a quarter
 // overlaps the copy of the previous one. Named barriers: kBarFull + b (staged -> copy) and
@@ -479,10 +479,14 @@ __device__ __forceinline__ void copy_quarter(const KernelArgs& a, const uint8_t*
                            pack_bf16x2(__uint_as_float(x.z), __uint_as_float(x.w)));
         }
     } else {
-        float* base = a.part_out + (static_cast<int64_t>(row) * a.splits + split) * a.h_q * 512 + 128 * qt + 4 * lane;
+        uint16_t* base = a.part_out + (static_cast<int64_t>(row) * a.splits + split) * a.h_q * 512 + 128 * qt + 4 * lane;
 #pragma unroll 2
-        for (int hh = wi; hh < a.h_q; hh += kConvWarps)
-            *reinterpret_cast<uint4*>(base + static_cast<int64_t>(hh) * 512) = lds_u128(b + hh * 512 + ((lane ^ (hh & 7)) << 4));
+        for (int hh = wi; hh < a.h_q; hh += kConvWarps) {
+            const uint4 x = lds_u128(b + hh * 512 + ((lane ^ (hh & 7)) << 4));
+            *reinterpret_cast<uint2*>(base + static_cast<int64_t>(hh) * 512) =
+                make_uint2(pack_f16x2(__uint_as_float(x.x), __uint_as_float(x.y)),
+                           pack_f16x2(__uint_as_float(x.z), __uint_as_float(x.w)));
+        }
     }
 }
 
@@ -908,7 +912,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) sparse_
 // the decode kernel: out = sum_s w_s part_s with w_s = 2^{lse2_s} / (sum_s 2^{lse2_s} + e^{sink}),
 // lse = ln sum_s e^{lse_s} (the sink is not part of lse); lse2 = log2-domain partial lse. Lane s
 // holds splits s and s + 32; lane l accumulates columns 4l + 128k (k = 0..3).
-__global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ part_out,
+__global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict__ part_out,
                                                       const float* __restrict__ part_lse, int splits, int h_q,
                                                       int rows_heads, const float* __restrict__ sink,
                                                       __nv_bfloat16* __restrict__ out, float* __restrict__ lse) {
@@ -938,14 +942,16 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
         const float w0 = e0 * inv, w1 = e1 * inv;
         for (int sp = 0; sp < splits; ++sp) {
             const float w = __shfl_sync(0xffffffffu, sp < 32 ? w0 : w1, sp & 31);
-            const float* src = part_out + ((base + sp) * h_q + h) * 512 + 4 * lane;
+            const uint16_t* src = part_out + ((base + sp) * h_q + h) * 512 + 4 * lane;
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-                const float4 v = *reinterpret_cast<const float4*>(src + 128 * k);
-                acc[k].x += w * v.x;
-                acc[k].y += w * v.y;
-                acc[k].z += w * v.z;
-                acc[k].w += w * v.w;
+                const uint2 u = *reinterpret_cast<const uint2*>(src + 128 * k);   // four f16
+                const float2 lo = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
+                const float2 hi = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
+                acc[k].x += w * lo.x;
+                acc[k].y += w * lo.y;
+                acc[k].z += w * hi.x;
+                acc[k].w += w * hi.y;
             }
         }
     }
@@ -1074,7 +1080,7 @@ cudaError_t launch_sparse_decode(const DecodeArgs& d, cudaStream_t stream) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, combine_kernel, static_cast<const float*>(d.part_out),
+    return cudaLaunchKernelEx(&cfg, combine_kernel, static_cast<const uint16_t*>(d.part_out),
                               static_cast<const float*>(d.part_lse), d.splits, d.h_q, rows_heads, d.attn_sink,
                               static_cast<__nv_bfloat16*>(d.out), d.lse);
 }

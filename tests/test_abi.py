@@ -54,7 +54,7 @@ def test_host_side_checks_return_codes_without_a_device(cdll):
     # an explicit split count needs no device: workspace = partial outputs + lse (256-B padded)
     assert cdll.nvfp4_sparse_mla_decode_workspace_size(2, 1, 64, 64, 352, 1, ctypes.byref(n)) == lib.OK and n.value == 0
     assert cdll.nvfp4_sparse_mla_decode_workspace_size(2, 1, 64, 64, 352, 2, ctypes.byref(n)) == lib.OK
-    assert n.value == 2 * 2 * 64 * 512 * 4 + 1024
+    assert n.value == 2 * 2 * 64 * 512 * 2 + 1024
     # quantize_append: zero tokens is a no-op; bad record width / null pointers are errors
     assert cdll.nvfp4_mla_quantize_append(None, 512, None, 64, None, 0, None, 0, 352, None, None) == lib.OK
     assert cdll.nvfp4_mla_quantize_append(None, 512, None, 64, None, 4, None, 8, 352, None, None) == lib.ERR_INVALID_ARG

@@ -61,12 +61,12 @@ def test_no_alloc_matches_the_workspace_entry_point_on_two_calls_in_a_row():
 def test_no_alloc_rejects_problems_beyond_its_scratch_limit():
     cdll = lib.load(build_if_missing=True)
     limit = 32 << 20
-    # 64 splits x 128 heads x 512 fp32 per row is 16 MiB: three rows need more than the limit
-    assert lib.workspace_size(3, 1, 128, 4096, 352, 64) > limit
-    q = torch.zeros((3, 1, 128, 576), dtype=torch.bfloat16, device=DEV)
-    idx = torch.zeros((3, 1, 4096), dtype=torch.int32, device=DEV)
+    # 64 splits x 128 heads x 512 f16 per row is 8 MiB: five rows need more than the limit
+    assert lib.workspace_size(5, 1, 128, 4096, 352, 64) > limit
+    q = torch.zeros((5, 1, 128, 576), dtype=torch.bfloat16, device=DEV)
+    idx = torch.zeros((5, 1, 4096), dtype=torch.int32, device=DEV)
     cache = torch.zeros((16, 352), dtype=torch.uint8, device=DEV)
-    out = torch.zeros((3, 1, 128, 512), dtype=torch.bfloat16, device=DEV)
-    lse = torch.zeros((3, 1, 128), dtype=torch.float32, device=DEV)
+    out = torch.zeros((5, 1, 128, 512), dtype=torch.bfloat16, device=DEV)
+    lse = torch.zeros((5, 1, 128), dtype=torch.float32, device=DEV)
     st = _no_alloc(cdll, q, cache, idx, 0.1, None, out, lse, 64, None)
     assert st == lib.ERR_WORKSPACE
