@@ -80,6 +80,9 @@ quantize_append_kernel(const uint16_t* __restrict__ latent, int64_t latent_strid
                        int64_t rope_stride, const int64_t* __restrict__ slot_mapping, int64_t num_tokens,
                        uint8_t* __restrict__ cache, int64_t num_slots, uint32_t* __restrict__ dev_status) {
     __shared__ __align__(16) uint8_t stage[kWarpsPerBlock][R];
+    // A decode launched next on the stream may start its prologue now; it waits for this grid
+    // before it reads anything.
+    asm volatile("griddepcontrol.launch_dependents;");
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     uint8_t* rec = stage[warp];

@@ -586,6 +586,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) sparse_
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = ctl->tmem_base;
+    // Launched as a programmatic dependent of the preceding kernel (typically the append that
+    // wrote the newest records): the prologue above overlaps its tail; nothing is read before
+    // that grid has completed and its writes are visible.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;");   // the split merge may be scheduled now
     // Every thread arrives on the cluster barrier now (barriers of both CTAs initialized); only
     // the threads that touch the peer CTA wait on it before their first remote access, the
@@ -1056,17 +1060,23 @@ cudaError_t launch_sparse_decode(const DecodeArgs& d, cudaStream_t stream) {
     a.status = d.dev_status;
     const dim3 grid(static_cast<unsigned>(d.rows) * static_cast<unsigned>(d.splits) * 2u);
     const dim3 block(kThreads);
-    cudaError_t err;
-    if (d.record_bytes == 352) {
-        err = prepare_kernel<352>();
-        if (err != cudaSuccess) return err;
-        sparse_decode_kernel<352><<<grid, block, SmemSize<352>::value, stream>>>(a);
-    } else {
-        err = prepare_kernel<432>();
-        if (err != cudaSuccess) return err;
-        sparse_decode_kernel<432><<<grid, block, SmemSize<432>::value, stream>>>(a);
+    cudaError_t err = d.record_bytes == 352 ? prepare_kernel<352>() : prepare_kernel<432>();
+    if (err != cudaSuccess) return err;
+    {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = grid;
+        cfg.blockDim = block;
+        cfg.dynamicSmemBytes = d.record_bytes == 352 ? SmemSize<352>::value : SmemSize<432>::value;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // see griddepcontrol.wait
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        err = d.record_bytes == 352 ? cudaLaunchKernelEx(&cfg, sparse_decode_kernel<352>, a)
+                                    : cudaLaunchKernelEx(&cfg, sparse_decode_kernel<432>, a);
     }
-    err = cudaGetLastError();
+    if (err == cudaSuccess) err = cudaGetLastError();
     if (err != cudaSuccess || d.splits == 1) return err;
     // the merge launches while the decode grid runs and waits for it on the device
     cudaLaunchConfig_t cfg = {};
