@@ -330,42 +330,64 @@ def run_gpu(args):
     decode_s = statistics.mean(decode_ms) / 1e3
     clocks = sampler.summary()
 
-    # ---- end to end through the public API with host buffers
+    # ---- end to end through the public API with host buffers: every step copies its inputs in
+    # from pinned host memory and its result out. Device inputs and outputs are double-buffered
+    # over three streams (copy in, compute, copy out), so step k+1's upload and step k-1's
+    # download overlap step k's kernels, as a caller pipelining these calls would.
     pin = lambda t: t.pin_memory()
     host_q = [pin(s.q) for s in sets]
     host_idx = [pin(s.indices) for s in sets]
     host_new = [tuple(pin(t) for t in new_token_batch(w0, k)) for k in range(N_SETS)]
-    host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    host_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
-    d_q = torch.empty_like(qs[0])
-    d_idx = torch.empty_like(idxs[0])
-    d_new = [torch.empty_like(t) for t in news[0]]
+    host_out = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(2)]
+    host_lse = [torch.empty(lse.shape, dtype=lse.dtype).pin_memory() for _ in range(2)]
+    d_q = [torch.empty_like(qs[0]) for _ in range(2)]
+    d_idx = [torch.empty_like(idxs[0]) for _ in range(2)]
+    d_new = [[torch.empty_like(t) for t in news[0]] for _ in range(2)]
+    d_out = [torch.empty_like(out) for _ in range(2)]
+    d_lse = [torch.empty_like(lse) for _ in range(2)]
+    s_in, s_comp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in range(2)]     # inputs of buffer b uploaded
+    ev_used = [torch.cuda.Event() for _ in range(2)]   # kernels done with buffer b
+    ev_out = [torch.cuda.Event() for _ in range(2)]    # result of buffer b downloaded
+    for e in ev_used + ev_out:
+        e.record(stream)
 
     def e2e_step(k):
-        j = k % N_SETS
-        d_q.copy_(host_q[j], non_blocking=True)
-        d_idx.copy_(host_idx[j], non_blocking=True)
-        for d, h in zip(d_new, host_new[j]):
-            d.copy_(h, non_blocking=True)
-        lib.quantize_append(d_new[0], d_new[1], d_new[2], cache, stream=stream)
-        lib.sparse_mla_decode(d_q, cache, d_idx, w0.sm_scale, out=out, lse=lse, num_splits=splits,
-                              workspace=workspace, stream=stream)
-        host_out.copy_(out, non_blocking=True)
-        host_lse.copy_(lse, non_blocking=True)
+        j, b = k % N_SETS, k % 2
+        with torch.cuda.stream(s_in):
+            s_in.wait_event(ev_used[b])
+            d_q[b].copy_(host_q[j], non_blocking=True)
+            d_idx[b].copy_(host_idx[j], non_blocking=True)
+            for d, h in zip(d_new[b], host_new[j]):
+                d.copy_(h, non_blocking=True)
+            ev_in[b].record(s_in)
+        s_comp.wait_event(ev_in[b])
+        s_comp.wait_event(ev_out[b])
+        lib.quantize_append(d_new[b][0], d_new[b][1], d_new[b][2], cache, stream=s_comp)
+        lib.sparse_mla_decode(d_q[b], cache, d_idx[b], w0.sm_scale, out=d_out[b], lse=d_lse[b],
+                              num_splits=splits, workspace=workspace, stream=s_comp)
+        ev_used[b].record(s_comp)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev_used[b])
+            host_out[b].copy_(d_out[b], non_blocking=True)
+            host_lse[b].copy_(d_lse[b], non_blocking=True)
+            ev_out[b].record(s_out)
 
     for k in range(args.warmup):
         e2e_step(k)
     torch.cuda.synchronize()
     barrier(world)
     s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    s2.record(stream)
+    s2.record(s_in)
     for k in range(args.steps):
         e2e_step(k)
-    e2.record(stream)
+    for s_ in (s_comp, s_out):
+        s_in.wait_stream(s_)
+    e2.record(s_in)
     torch.cuda.synchronize()
     t_e2e = max_over_ranks(s2.elapsed_time(e2) / 1e3, world, dev)
     h2d = sum(t.numel() * t.element_size() for t in (host_q[0], host_idx[0]) + host_new[0])
-    d2h = host_out.numel() * host_out.element_size() + host_lse.numel() * host_lse.element_size()
+    d2h = host_out[0].numel() * host_out[0].element_size() + host_lse[0].numel() * host_lse[0].element_size()
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {int(status.item())} after timing")
 
