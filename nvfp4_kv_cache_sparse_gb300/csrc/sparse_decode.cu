@@ -29,8 +29,8 @@
 //   CTA 0: warps 0-7 softmax (warp w: TMEM lanes 32 (w & 3).., score columns 32 (w >> 2)..+32;
 //          the two column halves exchange tile maxima), warps 24-25 QK issuers (even / odd
 //          tiles; one elected lane each).
-//   CTA 1: warps 0-3 rescale O and stage the output (thread r = TMEM lane r), warp 24 PV
-//          issuer; the converter warps copy the staged output out.
+//   CTA 1: warps 0-3 rescale O (thread r = TMEM lane r), warps 0-7 stage the output, warp 24
+//          PV issuer; the converter warps copy the staged output out.
 // Tiles are 64 keys; every K/V tile is written in a 128B-swizzled layout that is the K-major
 // B operand of QK (CTA 0) or the MN-major B operand of PV (CTA 1).
 //
@@ -454,12 +454,13 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t threads) {
 
 // Output of CTA 1: O * factor for the row's 128 x 512 block goes out (bf16 `out` when there is
 // one split, the split's f16 partial otherwise) through shared memory, so every warp store
-// covers whole 128-byte lines. Four quarters of 128 columns are staged in the two V stages alternately (row h
-// at h * 512, 16-byte chunk k at slot k ^ (h & 7)) by warps 0-3 (thread h = TMEM lane h) and
-// copied out by the converter warps (one row per warp instruction), so staging of a quarter
-// overlaps the copy of the previous one. Named barriers: kBarFull + b (staged -> copy) and
-// kBarEmpty + b (copied -> restage), b = quarter & 1, each counting all kOutThreads threads.
-constexpr int kOutThreads = 128 + 32 * kConvWarps;
+// covers whole 128-byte lines. Four quarters of 128 columns are staged in the two V stages
+// alternately (row h at h * 512, 16-byte chunk k at slot k ^ (h & 7)) by warps 0-7 (warps w and
+// w + 4 serve TMEM lanes 32w.., each half of the columns) and copied out by the converter warps
+// (one row per warp instruction), so staging of a quarter overlaps the copy of the previous
+// one. Named barriers: kBarFull + b (staged -> copy) and kBarEmpty + b (copied -> restage),
+// b = quarter & 1, each counting all kOutThreads threads.
+constexpr int kOutThreads = 256 + 32 * kConvWarps;
 constexpr uint32_t kBarFull = 2;
 constexpr uint32_t kBarEmpty = 4;
 
@@ -490,14 +491,16 @@ __device__ __forceinline__ void copy_quarter(const KernelArgs& a, const uint8_t*
     }
 }
 
-// Warps 0-3: stage each quarter once the copy of the quarter before last has left its buffer.
-__device__ __forceinline__ void write_rows(uint8_t* smem, uint32_t lane_base, bool use_o, float factor, int h) {
+// Warps 0-7 (TMEM lane quadrant w & 3): stage 64 of each quarter's 128 columns (from c0 * 32)
+// once the copy of the quarter before last has left its buffer.
+__device__ __forceinline__ void write_rows(uint8_t* smem, uint32_t lane_base, bool use_o, float factor, int h,
+                                           int c0) {
 #pragma unroll 1
     for (int qt = 0; qt < 4; ++qt) {
         const uint32_t buf = smem_addr(smem + kOffV + (qt & 1) * kVTileBytes);
         if (qt >= 2) named_bar_sync(kBarEmpty + (qt & 1), kOutThreads);
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
+        for (int c = c0; c < c0 + 2; ++c) {
             uint32_t o[32];
             if (use_o) {
                 tmem_ld32(lane_base + kColO + 128 * qt + 32 * c, o);
@@ -795,13 +798,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) sparse_
             if (!mbar_wait(&ctl->drain, 0)) set_abort(ctl, a.status);
         }
     } else {
-        if (warp < 4) {
-            // ============ CTA 1, warps 0-3: per-tile alpha check / O rescale, then the output ============
-            const int h = threadIdx.x;
-            const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+        if (warp < 8) {
+            // ============ CTA 1, warps 0-3: per-tile alpha check / O rescale; warps 0-7: the output ============
+            const int quad = warp & 3;
+            const bool second = warp >= 4;   // warps 4-7 only help stage the output
+            const int h = quad * 32 + lane;
+            const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
             const float* s_alpha = reinterpret_cast<const float*>(smem + kOffAlpha);
             bool ok = true;
-            for (int i = 0; i < n_tiles && ok; ++i) {
+            for (int i = 0; i < n_tiles && ok && !second; ++i) {
                 const int ps = i % kPStages;
                 if (lane == 0) mbar_arrive_expect_tx(&ctl->pfull[ps], 32 * (128 + 4));
                 ok = wait_warp(ctl, &ctl->pfull[ps], (i / kPStages) & 1, a.status);
@@ -827,7 +832,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) sparse_
                 mbar_arrive(&ctl->ready[ps]);
             }
             // ---- output
-            if (lane == 0) mbar_arrive_expect_tx(&ctl->fin, 32 * 8);
+            if (!second && lane == 0) mbar_arrive_expect_tx(&ctl->fin, 32 * 8);
             const bool have_fin = ok && wait_warp(ctl, &ctl->fin, 0, a.status);
             bool have_o = false;
             if (have_fin && n_tiles > 0) {
@@ -849,13 +854,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) sparse_
                     denom += exp2f(__ldg(a.sink + (h < a.h_q ? h : 0)) * kLog2e - m_ref);
                 factor = 1.0f / denom;
             }
-            if (h < a.h_q) {
+            if (h < a.h_q && !second) {
                 if (a.splits == 1)
                     a.lse[static_cast<int64_t>(row) * a.h_q + h] = lse2 * kLn2;
                 else
                     a.part_lse[(static_cast<int64_t>(row) * a.splits + split) * a.h_q + h] = lse2;
             }
-            write_rows(smem, lane_base, have_o && !empty, factor, h);
+            write_rows(smem, lane_base, have_o && !empty, factor, h, second ? 2 : 0);
         } else if (converter) {
             // ============ CTA 1, warps 8-23: dequant of the NoPE halves (V tiles) ============
             convert_tiles<R, false, kVStages, kVTileBytes, RawRing<R>::kStages1>(
@@ -866,7 +871,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) sparse_
             produce_raw<R, false, RawRing<R>::kStages1>(a, ctl, smem + kOffRaw1, idx_row, key_begin, key_end, n_tiles,
                                                         warp - kWarpProd, lane);
         } else if (warp == kWarpMma) {
-            // ============ CTA 1, warp 24: PV issuer (warps 4-7 and 25 idle) ============
+            // ============ CTA 1, warp 24: PV issuer (warp 25 idle) ============
             cluster_wait();          // CTA 0's pempty barriers exist before the first multicast commit
             const uint32_t idesc_pv = idesc_f16_f32(kHeadsM, 256, false, true);
             const uint64_t pdesc0 = sdesc_sw128(smem_addr(smem + kOffP), 16, 1024);
