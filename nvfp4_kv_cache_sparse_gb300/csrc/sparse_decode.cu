@@ -61,7 +61,6 @@ constexpr int kVStages = 2;                        // CTA 1: V tiles of 8 blocks
 constexpr int kVTileBytes = 8 * kBlkBytes;         // 64 KB
 constexpr int kPStages = 2;                        // CTA 1: P tiles [128 heads x 64 keys] f16
 constexpr int kPBytes = kHeadsM * 128;             // 16 KB
-constexpr int kMaskSlots = 16;
 // Raw-record ring, filled by TMA tile::gather4 (four whole records per instruction, each group of
 // four starting on a 128-byte boundary): CTA 0 keeps 3 tiles in flight for 352-byte records and
 // 2 for 432-byte records, CTA 1 keeps 2.
@@ -96,7 +95,6 @@ struct __align__(8) SmemCtl {
     uint64_t kempty[kKStages];    // QK commit -> dequant
     uint64_t sfull[2];            // QK commit -> softmax
     uint64_t sfree[2];            // softmax has read S -> QK issuer
-    uint64_t mfull[kMaskSlots];   // used-key mask of a tile written (producer warps)
     uint64_t pempty[kPStages];    // CTA 1's PV has read the P slot (multicast commit)
     uint64_t qload;               // CTA 0: Q's nine 64-column boxes landed in shared memory (TMA)
     uint64_t qready;              // Q in TMEM
@@ -112,7 +110,6 @@ struct __align__(8) SmemCtl {
     uint64_t rawfull[kMaxRawStages];    // producer warps: expect_tx + gather4 bytes -> converters
     uint64_t rawempty[kMaxRawStages];   // converter warps (one arrival each) -> producers
     uint32_t rawvalid[kMaxRawStages][2];   // used-key bits of the tile in each raw slot
-    uint32_t mask[kMaskSlots][2];          // CTA 0: used-key bits of tile i (slot i % kMaskSlots)
     uint64_t xbar[2];             // CTA 0: both softmax halves posted their tile max (tile parity)
     uint64_t lbar;                // CTA 0: softmax half 1 posted its final row sum
     uint32_t tmem_base;
@@ -140,7 +137,6 @@ struct SmemSize {
 };
 static_assert(SmemSize<352>::value <= 232448 && SmemSize<432>::value <= 232448, "shared memory");
 static_assert(kOffRaw0 % 128 == 0 && kOffRaw1 % 128 == 0, "gather4 destinations are 128-byte aligned");
-static_assert(offsetof(SmemCtl, mask) % 8 == 0, "a tile's mask is read as one 64-bit word");
 
 struct KernelArgs {
     CUtensorMap tmap;            // the cache as u32 [num_slots, R / 4], box one record
@@ -274,7 +270,7 @@ __device__ __forceinline__ bool wait_warp(SmemCtl* ctl, uint64_t* bar, uint32_t 
 // tile. Eight threads share a key: thread (q, hi) = (sub & 3, sub >> 2) converts the 16-wide NoPE
 // blocks 4c+q for c = 4hi..4hi+3 (their four scales are bytes 8q+4hi.. of the permuted scale field
 // of a 352-byte record: one 4-byte load) and RoPE dims [8 sub, 8 sub + 8). A masked key writes
-// zeros.
+// zeros in a V tile and quiet NaNs in a K tile.
 template <int R, bool kRope>
 __device__ __forceinline__ void convert_part(uint32_t rec, bool valid, uint32_t tile, int key, int sub) {
     const int q = sub & 3;
@@ -320,7 +316,10 @@ __device__ __forceinline__ void convert_part(uint32_t rec, bool valid, uint32_t 
             sts_u128(tile + 8 * kBlkBytes + swz(key, sub), r);
         }
     } else {
-        const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+        // A masked key: zeros in a V tile; quiet NaNs in a K tile, so that every score of the
+        // key comes out NaN and the softmax drops it without reading a mask.
+        const uint32_t f = kRope ? 0x7FC07FC0u : 0u;
+        const uint4 z = make_uint4(f, f, f, f);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             const int c = 4 * hi + j;
@@ -374,10 +373,6 @@ __device__ __forceinline__ void produce_raw(const KernelArgs& a, SmemCtl* ctl, u
         const uint32_t groups = __popc(__ballot_sync(0xffffffffu, lane < 8 && bits != 0u));
         if (lane == 0) {
             ctl->rawvalid[rs][pw] = word;
-            if (kRope) {
-                ctl->mask[j % kMaskSlots][pw] = word;
-                mbar_arrive(&ctl->mfull[j % kMaskSlots]);
-            }
             mbar_arrive_expect_tx(&ctl->rawfull[rs], groups * 4u * R);
         }
         __syncwarp();
@@ -563,7 +558,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) sparse_
             mbar_init(&ctl->odone[i], 1);
             mbar_init(&ctl->xbar[i], 256);
         }
-        for (int i = 0; i < kMaskSlots; ++i) mbar_init(&ctl->mfull[i], kProducerWarps);
         for (int i = 0; i < kMaxRawStages; ++i) {
             mbar_init(&ctl->rawfull[i], kProducerWarps);
             mbar_init(&ctl->rawempty[i], kConvWarps);
@@ -663,35 +657,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) sparse_
                 tmem_wait_ld();
                 tc_fence_before_sync();
                 mbar_arrive(&ctl->sfree[b]);
-                ok = wait_warp(ctl, &ctl->mfull[i % kMaskSlots], (i / kMaskSlots) & 1, a.status);
-                if (!ok) break;
-                const uint32_t used = *reinterpret_cast<const volatile uint32_t*>(&ctl->mask[i % kMaskSlots][half]);
                 // ---- online softmax (log2 domain, lazy reference max): z = s * scale_log2.
-                // Common case (every key used, scale > 0): the max is taken on the raw scores and
-                // each z - m is one fused multiply-add; otherwise masked keys become -inf first.
+                // A masked key's scores are NaN (its K row is NaN): max ignores them, and
+                // max(z, -inf) turns their z into -inf, whose exponential is 0.
                 float zs = a.scale_log2;      // multiplier applied to s[] below
                 float part_max;
-                if (used == 0xFFFFFFFFu && zs > 0.0f) {
+                {
                     float m0 = -INFINITY, m1 = -INFINITY;
+                    if (zs > 0.0f) {
 #pragma unroll
-                    for (int j = 0; j < 32; j += 4) {
-                        m0 = fmax3(m0, __uint_as_float(s[j]), __uint_as_float(s[j + 1]));
-                        m1 = fmax3(m1, __uint_as_float(s[j + 2]), __uint_as_float(s[j + 3]));
-                    }
-                    part_max = fmaxf(m0, m1) * zs;
-                } else {
-                    float m0 = -INFINITY, m1 = -INFINITY;
+                        for (int j = 0; j < 32; j += 4) {
+                            m0 = fmax3(m0, __uint_as_float(s[j]), __uint_as_float(s[j + 1]));
+                            m1 = fmax3(m1, __uint_as_float(s[j + 2]), __uint_as_float(s[j + 3]));
+                        }
+                        part_max = fmaxf(m0, m1) * zs;
+                    } else {
 #pragma unroll
-                    for (int j = 0; j < 32; j += 2) {
-                        const float v0 = ((used >> j) & 1u) ? __uint_as_float(s[j]) * zs : -INFINITY;
-                        const float v1 = ((used >> (j + 1)) & 1u) ? __uint_as_float(s[j + 1]) * zs : -INFINITY;
-                        s[j] = __float_as_uint(v0);
-                        s[j + 1] = __float_as_uint(v1);
-                        m0 = fmaxf(m0, v0);
-                        m1 = fmaxf(m1, v1);
+                        for (int j = 0; j < 32; ++j) {
+                            const float v = __uint_as_float(s[j]) * zs;
+                            s[j] = __float_as_uint(v);
+                            m0 = fmaxf(m0, v);
+                        }
+                        part_max = m0;
+                        zs = 1.0f;
                     }
-                    part_max = fmaxf(m0, m1);
-                    zs = 1.0f;
                 }
                 // ---- tile max over both halves
                 xmax[(b * 2 + half) * kHeadsM + h] = part_max;
@@ -718,8 +707,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) sparse_
                                 f32x2_fma(f32x2_pack(__uint_as_float(s[j]), __uint_as_float(s[j + 1])), mul2, neg_m2));
                             const float2 z1 = f32x2_unpack(
                                 f32x2_fma(f32x2_pack(__uint_as_float(s[j + 2]), __uint_as_float(s[j + 3])), mul2, neg_m2));
-                            const float p0 = ex2_approx(z0.x), p1 = ex2_approx(z0.y);
-                            const float p2 = ex2_approx(z1.x), p3 = ex2_approx(z1.y);
+                            const float p0 = ex2_approx(fmaxf(z0.x, -INFINITY)), p1 = ex2_approx(fmaxf(z0.y, -INFINITY));
+                            const float p2 = ex2_approx(fmaxf(z1.x, -INFINITY)), p3 = ex2_approx(fmaxf(z1.y, -INFINITY));
                             la = f32x2_add(la, f32x2_pack(p0, p1));
                             lb = f32x2_add(lb, f32x2_pack(p2, p3));
                             p[(j & 7) / 2] = pack_f16x2(p0, p1);
