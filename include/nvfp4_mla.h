@@ -26,11 +26,12 @@
  *    No call allocates device memory. The only device memory the library owns is the
  *    fixed scratch array of nvfp4_sparse_mla_decode_no_alloc (see there).
  *  - `stream` is a cudaStream_t (NULL = the legacy default stream). Work is enqueued on it
- *    and the call returns without synchronizing. Stream order is kept as usual: the decode
- *    kernel is launched as a programmatic dependent of the preceding work on the stream, so its
- *    prologue (barrier setup, tensor-memory allocation) may overlap the preceding kernel's
- *    tail, but it reads no input before that kernel has completed and its writes are visible;
- *    nvfp4_mla_quantize_append lets a following dependent start its prologue at once.
+ *    and the call returns without synchronizing. Stream order is kept as usual: every kernel
+ *    of the library is launched as a programmatic dependent of the preceding work on the
+ *    stream, so its prologue (for the decode: barrier setup, tensor-memory allocation) may
+ *    overlap the preceding kernel's tail, but it reads and writes no memory before that kernel
+ *    has completed and its writes are visible. The library's kernels let the next kernel on
+ *    the stream start its prologue early in the same way.
  *  - Every argument check runs on the host before any launch; a failed check returns a
  *    status below and launches nothing. Kernels never trap: problems found on the device
  *    are OR-ed into *dev_status (if non-NULL) as NVFP4_MLA_DEV_* bits, readable after the

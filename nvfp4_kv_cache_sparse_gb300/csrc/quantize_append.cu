@@ -81,8 +81,10 @@ quantize_append_kernel(const uint16_t* __restrict__ latent, int64_t latent_strid
                        uint8_t* __restrict__ cache, int64_t num_slots, uint32_t* __restrict__ dev_status) {
     __shared__ __align__(16) uint8_t stage[kWarpsPerBlock][R];
     // A decode launched next on the stream may start its prologue now; it waits for this grid
-    // before it reads anything.
+    // before it reads anything. This grid is itself a programmatic dependent of the preceding
+    // kernel and waits for it to complete before reading or writing memory.
     asm volatile("griddepcontrol.launch_dependents;");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     uint8_t* rec = stage[warp];
@@ -168,16 +170,23 @@ cudaError_t launch_quantize_append(const void* kv_latent, int64_t latent_row_str
     const dim3 block(kWarpsPerBlock * 32);
     const auto* lat = static_cast<const uint16_t*>(kv_latent);
     const auto* rope = static_cast<const uint16_t*>(k_rope);
-    if (record_bytes == 352) {
-        quantize_append_kernel<352><<<grid, block, 0, stream>>>(lat, latent_row_stride, rope, rope_row_stride,
-                                                                slot_mapping, num_tokens, cache, num_slots,
-                                                                dev_status);
-    } else {
-        quantize_append_kernel<432><<<grid, block, 0, stream>>>(lat, latent_row_stride, rope, rope_row_stride,
-                                                                slot_mapping, num_tokens, cache, num_slots,
-                                                                dev_status);
-    }
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // see griddepcontrol.wait
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t err =
+        record_bytes == 352
+            ? cudaLaunchKernelEx(&cfg, quantize_append_kernel<352>, lat, latent_row_stride, rope, rope_row_stride,
+                                 slot_mapping, num_tokens, cache, num_slots, dev_status)
+            : cudaLaunchKernelEx(&cfg, quantize_append_kernel<432>, lat, latent_row_stride, rope, rope_row_stride,
+                                 slot_mapping, num_tokens, cache, num_slots, dev_status);
+    return err != cudaSuccess ? err : cudaGetLastError();
 }
 
 }  // namespace nvfp4mla
