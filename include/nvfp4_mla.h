@@ -30,8 +30,9 @@
  *    of the library is launched as a programmatic dependent of the preceding work on the
  *    stream, so its prologue (for the decode: barrier setup, tensor-memory allocation) may
  *    overlap the preceding kernel's tail, but it reads and writes no memory before that kernel
- *    has completed and its writes are visible. The library's kernels let the next kernel on
- *    the stream start its prologue early in the same way.
+ *    has completed and its writes are visible. The append and decode kernels let the next
+ *    kernel on the stream start its prologue early in the same way; the decode's split merge
+ *    does not (a waiting successor would hold the SMs the merge runs on).
  *  - Every argument check runs on the host before any launch; a failed check returns a
  *    status below and launches nothing. Kernels never trap: problems found on the device
  *    are OR-ed into *dev_status (if non-NULL) as NVFP4_MLA_DEV_* bits, readable after the

@@ -914,7 +914,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
                                                       const float* __restrict__ part_lse, int splits, int h_q,
                                                       int rows_heads, const float* __restrict__ sink,
                                                       __nv_bfloat16* __restrict__ out, float* __restrict__ lse) {
-    asm volatile("griddepcontrol.launch_dependents;");   // the next kernel may start its prologue
+    // No early trigger here: a decode launched next would park its CTAs on the SMs this grid
+    // needs while it waits for it.
     asm volatile("griddepcontrol.wait;" ::: "memory");   // the decode grid's partials are visible
     const int lane = threadIdx.x & 31;
     const int rh = blockIdx.x * 8 + (threadIdx.x >> 5);   // row * h_q + h
