@@ -167,6 +167,17 @@ NVFP4_MLA_API int nvfp4_sparse_mla_decode_no_alloc(const void* q, const uint8_t*
                                                    const float* attn_sink, void* out, float* lse,
                                                    int32_t num_splits, uint32_t* dev_status, void* stream);
 
+/*
+ * Self-test of the decode's wait bound (no counterpart on the pages). Every pipeline wait in
+ * the decode kernel gives up after about one second (then the kernel sets
+ * NVFP4_MLA_DEV_TIMEOUT, drains its own work and returns; the context stays usable). This call
+ * runs one such wait on an mbarrier that nothing arrives on, on `stream`:
+ *   dev_status   device uint32: NVFP4_MLA_DEV_TIMEOUT is OR-ed in when the wait gives up.
+ *   elapsed_ns   device uint64: how long the wait lasted, in nanoseconds.
+ * Returns NVFP4_MLA_ERR_INVALID_ARG for NULL pointers, NVFP4_MLA_ERR_UNSUPPORTED off sm_103.
+ */
+NVFP4_MLA_API int nvfp4_mla_selftest_wait_timeout(uint32_t* dev_status, uint64_t* elapsed_ns, void* stream);
+
 /* Static text for a status code (never NULL). */
 NVFP4_MLA_API const char* nvfp4_mla_status_string(int status);
 

@@ -34,6 +34,7 @@ EXPORTED = (
     "nvfp4_sparse_mla_decode_no_alloc",
     "nvfp4_mla_status_string",
     "nvfp4_mla_version",
+    "nvfp4_mla_selftest_wait_timeout",
 )
 
 _lib: Optional[ctypes.CDLL] = None
@@ -73,6 +74,8 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
     lib.nvfp4_mla_status_string.argtypes = [ctypes.c_int]
     lib.nvfp4_mla_version.restype = ctypes.c_int
     lib.nvfp4_mla_version.argtypes = []
+    lib.nvfp4_mla_selftest_wait_timeout.restype = ctypes.c_int
+    lib.nvfp4_mla_selftest_wait_timeout.argtypes = [P, P, P]
     _lib = lib
     return lib
 
@@ -162,3 +165,16 @@ def sparse_mla_decode(q: torch.Tensor, cache: torch.Tensor, indices: torch.Tenso
         _stream(stream))
     _check("nvfp4_sparse_mla_decode", st)
     return out, lse
+
+
+def selftest_wait_timeout(device=None, stream=None) -> Tuple[int, int]:
+    """Runs one of the decode's time-bounded pipeline waits on an mbarrier that nothing arrives
+    on. Returns (device status bits, nanoseconds the wait lasted); the status should hold
+    DEV_TIMEOUT and the time be about one second."""
+    device = torch.device("cuda") if device is None else torch.device(device)
+    status = torch.zeros(1, dtype=torch.int32, device=device)
+    elapsed = torch.zeros(1, dtype=torch.int64, device=device)
+    _check("nvfp4_mla_selftest_wait_timeout",
+           load().nvfp4_mla_selftest_wait_timeout(_ptr(status), _ptr(elapsed), _stream(stream)))
+    torch.cuda.synchronize(device)
+    return int(status.item()), int(elapsed.item())

@@ -168,6 +168,15 @@ NVFP4_MLA_API int nvfp4_sparse_mla_decode(const void* q, const uint8_t* cache, i
     return e == cudaSuccess ? NVFP4_MLA_OK : NVFP4_MLA_ERR_CUDA;
 }
 
+NVFP4_MLA_API int nvfp4_mla_selftest_wait_timeout(uint32_t* dev_status, uint64_t* elapsed_ns, void* stream) {
+    if (!dev_status || !elapsed_ns || !aligned(elapsed_ns, 8)) return NVFP4_MLA_ERR_INVALID_ARG;
+    int status = NVFP4_MLA_OK;
+    if (device_sm_count(&status) <= 0) return status;
+    const cudaError_t e =
+        nvfp4mla::launch_wait_timeout_probe(dev_status, elapsed_ns, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? NVFP4_MLA_OK : NVFP4_MLA_ERR_CUDA;
+}
+
 NVFP4_MLA_API const char* nvfp4_mla_status_string(int status) {
     switch (status) {
         case NVFP4_MLA_OK: return "ok";

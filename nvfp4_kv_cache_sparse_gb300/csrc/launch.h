@@ -35,5 +35,7 @@ struct DecodeArgs {
 // Keys of one split, rounded to whole tiles.
 int decode_keys_per_split(int topk, int splits);
 cudaError_t launch_sparse_decode(const DecodeArgs& a, cudaStream_t stream);
+// One time-bounded mbarrier wait that runs out (see nvfp4_mla_selftest_wait_timeout).
+cudaError_t launch_wait_timeout_probe(uint32_t* status, uint64_t* elapsed_ns, cudaStream_t stream);
 
 }  // namespace nvfp4mla

@@ -53,14 +53,27 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Waits for the phase with the given parity to complete. Gives up after `limit` polls
-// (each poll itself may suspend for a bounded time) and returns false, so no wait in these
-// kernels can spin forever.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t limit = (1u << 20)) {
-    for (uint32_t i = 0; i < limit; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Longest time any wait in these kernels may take (a whole decode takes well under a millisecond).
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
+
+// Waits for the phase with the given parity to complete. A poll may itself suspend the thread
+// for a system-dependent time, so the bound is on elapsed time: after kWaitLimitNs the wait
+// gives up and returns false, and no wait in these kernels can last longer than about a second.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (;;) {
+#pragma unroll 1
+        for (int k = 0; k < 64; ++k)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (global_ns() - t0 > kWaitLimitNs) return false;
     }
-    return false;
 }
 
 __device__ __forceinline__ void fence_barrier_init() {
@@ -249,12 +262,16 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t pa
     return ok != 0;
 }
 
-// Bounded wait with cluster-scope acquire (for barriers that a peer CTA arrives on).
-__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, uint32_t limit = (1u << 20)) {
-    for (uint32_t i = 0; i < limit; ++i) {
-        if (mbar_try_wait_cluster(bar, parity)) return true;
+// Time-bounded wait with cluster-scope acquire (for barriers that a peer CTA arrives on).
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (;;) {
+#pragma unroll 1
+        for (int k = 0; k < 64; ++k)
+            if (mbar_try_wait_cluster(bar, parity)) return true;
+        if (global_ns() - t0 > kWaitLimitNs) return false;
     }
-    return false;
 }
 
 // Whole-cluster barrier (every thread of every CTA of the cluster).

@@ -963,6 +963,21 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
     if (lane == 0) lse[rh] = total;
 }
 
+// One thread waits on an mbarrier that nothing arrives on, with the same time-bounded wait the
+// decode uses: the wait gives up, the kernel records NVFP4_MLA_DEV_TIMEOUT and the time it
+// waited, and returns normally.
+__global__ void wait_timeout_probe_kernel(uint32_t* status, uint64_t* elapsed_ns) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x != 0) return;
+    mbar_init(&bar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    const uint64_t t0 = global_ns();
+    const bool done = mbar_wait(&bar, 0);
+    const uint64_t t1 = global_ns();
+    if (!done) atomicOr(status, 0x4u);   // NVFP4_MLA_DEV_TIMEOUT
+    *elapsed_ns = t1 - t0;
+}
+
 }  // namespace
 
 int decode_keys_per_split(int topk, int splits) {
@@ -1034,6 +1049,11 @@ cudaError_t prepare_kernel() {
 }
 
 }  // namespace
+
+cudaError_t launch_wait_timeout_probe(uint32_t* status, uint64_t* elapsed_ns, cudaStream_t stream) {
+    wait_timeout_probe_kernel<<<1, 32, 0, stream>>>(status, elapsed_ns);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_sparse_decode(const DecodeArgs& d, cudaStream_t stream) {
     KernelArgs a;

@@ -221,3 +221,21 @@ def test_varlen_mtp_sink_sampled():
 
 def test_long_context_432_sampled():
     _sampled_parity(synth.long_context(seed=0), 6)
+
+
+def test_a_wait_that_runs_out_reports_a_timeout_and_leaves_the_context_usable():
+    """The decode's pipeline waits are bounded in time: one that nothing completes gives up after
+    about a second, sets DEV_TIMEOUT and lets the kernel return; the next decode runs normally."""
+    st, ns = lib.selftest_wait_timeout()
+    assert st & lib.DEV_TIMEOUT
+    assert 0.9e9 <= ns <= 10e9, ns
+    w = synth.tiny_decode(seed=3)
+    cache = fill_pool(lib.quantize_append, w.num_slots, w.record_bytes, w.pool_seed, DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out, lse = lib.sparse_mla_decode(w.q.to(DEV), cache, w.indices.to(DEV), w.sm_scale, dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    ref_out, ref_lse = oracle.sparse_mla_decode(synth.bf16_bits(w.q), oracle_pool(w.pool_seed, w.num_slots,
+                                                                                  w.record_bytes),
+                                                w.indices.numpy().reshape(1, -1), w.sm_scale)
+    assert_close(out, lse, ref_out, ref_lse)
