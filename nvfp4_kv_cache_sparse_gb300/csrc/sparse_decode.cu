@@ -253,6 +253,7 @@ __device__ __forceinline__ bool aborted(SmemCtl* ctl) {
 }
 
 __device__ __forceinline__ bool wait_or_abort(SmemCtl* ctl, uint64_t* bar, uint32_t parity, uint32_t* status) {
+    if (mbar_try_wait(bar, parity)) return true;   // the common case: already complete
     if (aborted(ctl)) return false;
     if (mbar_wait(bar, parity)) return true;
     set_abort(ctl, status);
