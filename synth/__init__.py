@@ -223,12 +223,36 @@ def long_context(seed: int = 0, B: int = 64, h_q: int = 128, topk: int = 2048, n
                           seq_lens=lens)
 
 
+def sparse_prefill(seed: int = 0, B: int = 2, s_q: int = 256, h_q: int = 128, topk: int = 2048,
+                   prefix: int = 16_384) -> DecodeWorkload:
+    """Sparse prefill / extend: each of B requests has `prefix` cached tokens plus s_q new ones
+    whose records are appended before attention; new token i (position prefix + i) attends to
+    topk distinct positions drawn uniformly from 0..prefix + i (causal). Each request owns
+    ceil((prefix + s_q) / 64) pages from a seeded permutation of the pool's pages."""
+    rng = np.random.default_rng(seed)
+    pages_per_req = (prefix + s_q + PAGE - 1) // PAGE
+    num_pages = B * pages_per_req
+    perm = rng.permutation(num_pages)
+    idx = np.full((B, s_q, topk), -1, dtype=np.int32)
+    for b in range(B):
+        table = perm[b * pages_per_req:(b + 1) * pages_per_req]
+        for i in range(s_q):
+            visible = prefix + i + 1
+            n = min(visible, topk)
+            idx[b, i, :n] = _positions_to_slots(table, rng.choice(visible, size=n, replace=False))
+    q = _normal_bf16(rng, (B, s_q, h_q, D_QK))
+    return DecodeWorkload(f"prefill_b{B}_sq{s_q}_h{h_q}_topk{topk}_prefix{prefix}_R352", B, s_q, h_q, topk, 352,
+                          num_pages * PAGE, 1.0 / math.sqrt(D_QK), q, torch.from_numpy(idx), None,
+                          pool_seed=seed + 4000, seq_lens=np.full(B, prefix + s_q))
+
+
 WORKLOADS = {
     "tiny": tiny_decode,
     "write": write_path,
     "decode": batch_decode,
     "varlen": varlen_decode,
     "longctx": long_context,
+    "prefill": sparse_prefill,
 }
 
 

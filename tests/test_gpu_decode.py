@@ -219,6 +219,11 @@ def test_varlen_mtp_sink_sampled():
     _sampled_parity(synth.varlen_decode(seed=0), 8)
 
 
+def test_sparse_prefill_sampled():
+    """Sparse prefill / extend: 2 requests x 256 new tokens, causal top-k over a 16K prefix."""
+    _sampled_parity(synth.sparse_prefill(seed=0), 6)
+
+
 def test_long_context_432_sampled():
     _sampled_parity(synth.long_context(seed=0), 6)
 
