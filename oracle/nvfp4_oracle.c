@@ -20,7 +20,7 @@
  *                scale 1.0, zeroed pad, verbatim 16-bit RoPE) and "Tests" (scale =
  *                E4M3(group_amax/6), the E2M1 nibble table).
  *
- * Readings of points the pages leave open (each one is listed in the design doc):
+ * Readings of points the pages leave open:
  *  - e4m3 is the "fn" variant: no infinities, 0x7F/0xFF are NaN, largest finite 448.
  *  - Rounding is round-to-nearest, ties to the code whose least significant bit is 0,
  *    saturating to the largest finite magnitude; the sign of the input is kept, so a
