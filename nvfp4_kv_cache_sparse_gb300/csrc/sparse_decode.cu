@@ -488,7 +488,7 @@ __device__ __forceinline__ void copy_quarter(const KernelArgs& a, const uint8_t*
 }
 
 // Warps 0-7 (TMEM lane quadrant w & 3): stage 64 of each quarter's 128 columns (from c0 * 32)
-// once the copy of the quarter before last has left its buffer.
+// once the copy of the quarter before last has left its buffer. use_o must be warp-uniform.
 __device__ __forceinline__ void write_rows(uint8_t* smem, uint32_t lane_base, bool use_o, float factor, int h,
                                            int c0) {
 #pragma unroll 1
@@ -850,7 +850,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) sparse_
                 else
                     a.part_lse[(static_cast<int64_t>(row) * a.splits + split) * a.h_q + h] = lse2;
             }
-            write_rows(smem, lane_base, have_o && !empty, factor, h, second ? 2 : 0);
+            // have_o is the same in every lane of the warp (tcgen05.ld in write_rows is
+            // warp-collective); an empty row has factor 0 and an all-zero O row
+            write_rows(smem, lane_base, have_o, factor, h, second ? 2 : 0);
         } else if (converter) {
             // ============ CTA 1, warps 8-23: dequant of the NoPE halves (V tiles) ============
             convert_tiles<R, false, kVStages, kVTileBytes, RawRing<R>::kStages1>(
