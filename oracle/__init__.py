@@ -58,15 +58,15 @@ def lib() -> ctypes.CDLL:
         _lib.oracle_e2m1_encode.restype = ctypes.c_uint8
         _lib.oracle_e2m1_encode.argtypes = [ctypes.c_float]
         _lib.oracle_scale_offset.restype = i32
-        _lib.oracle_scale_offset.argtypes = [i32, i32]
+        _lib.oracle_scale_offset.argtypes = [i32, i32, i32]
         _lib.oracle_quantize_record.restype = None
-        _lib.oracle_quantize_record.argtypes = [P, P, i32, P]
+        _lib.oracle_quantize_record.argtypes = [P, P, i32, i32, P]
         _lib.oracle_quantize_append.restype = i64
-        _lib.oracle_quantize_append.argtypes = [P, i64, P, i64, P, i64, P, i64, i32]
+        _lib.oracle_quantize_append.argtypes = [P, i64, P, i64, P, i64, P, i64, i32, i32]
         _lib.oracle_dequant_records.restype = None
-        _lib.oracle_dequant_records.argtypes = [P, i64, i32, P]
+        _lib.oracle_dequant_records.argtypes = [P, i64, i32, i32, P]
         _lib.oracle_sparse_mla_decode.restype = None
-        _lib.oracle_sparse_mla_decode.argtypes = [P, P, i64, i32, P, i64, i64, i32, i32, d, P, P, i64, P, P, i32]
+        _lib.oracle_sparse_mla_decode.argtypes = [P, P, i64, i32, i32, P, i64, i64, i32, i32, d, P, P, i64, P, P, i32]
         _lib.oracle_merge_partials.restype = None
         _lib.oracle_merge_partials.argtypes = [i32, P, P, P, P, P]
         for name, intype, outtype in (("oracle_e4m3_encode_many", P, P), ("oracle_e2m1_encode_many", P, P),
@@ -118,15 +118,25 @@ def e2m1_decode(nibble: int) -> float:
     return float(lib().oracle_e2m1_decode(int(nibble)))
 
 
-def scale_offset(record_bytes: int, g: int) -> int:
-    return int(lib().oracle_scale_offset(int(record_bytes), int(g)))
+def _block_flag(record_bytes: int, block_scales: bool) -> int:
+    # the 432-byte record keeps its scales in block order by definition
+    assert not (block_scales and record_bytes != 352), "block_scales applies to the 352-byte record"
+    return 1 if block_scales else 0
+
+
+def scale_offset(record_bytes: int, g: int, block_scales: bool = False) -> int:
+    """Byte offset of block g's scale. ``block_scales``: the 352-byte record with its scales in
+    block order (the unpermuted side of the scale-layout comparison)."""
+    return int(lib().oracle_scale_offset(int(record_bytes), _block_flag(record_bytes, block_scales), int(g)))
 
 
 # ---- write side -----------------------------------------------------------------------
 
-def quantize_records(latent_bits: np.ndarray, rope_bits: np.ndarray, record_bytes: int) -> np.ndarray:
+def quantize_records(latent_bits: np.ndarray, rope_bits: np.ndarray, record_bytes: int,
+                     block_scales: bool = False) -> np.ndarray:
     """bf16 bits [T,512] and [T,64] -> records uint8 [T, record_bytes]."""
     assert record_bytes in RECORD_BYTES
+    blk = _block_flag(record_bytes, block_scales)
     lat = _c(latent_bits, np.uint16)
     rope = _c(rope_bits, np.uint16)
     T = lat.shape[0]
@@ -134,12 +144,12 @@ def quantize_records(latent_bits: np.ndarray, rope_bits: np.ndarray, record_byte
     out = np.zeros((T, record_bytes), dtype=np.uint8)
     L = lib()
     for t in range(T):
-        L.oracle_quantize_record(_ptr(lat[t]), _ptr(rope[t]), record_bytes, _ptr(out[t]))
+        L.oracle_quantize_record(_ptr(lat[t]), _ptr(rope[t]), record_bytes, blk, _ptr(out[t]))
     return out
 
 
 def quantize_append(latent_bits: np.ndarray, rope_bits: np.ndarray, slot_mapping: np.ndarray,
-                    cache: np.ndarray) -> int:
+                    cache: np.ndarray, block_scales: bool = False) -> int:
     """In-place write into ``cache`` (uint8 [num_slots, record_bytes]). Rows of ``latent_bits``
     and ``rope_bits`` may be strided views (element strides, inner stride 1). Returns the
     count of slots >= num_slots (skipped)."""
@@ -152,15 +162,15 @@ def quantize_append(latent_bits: np.ndarray, rope_bits: np.ndarray, slot_mapping
     T = slots.size
     return int(lib().oracle_quantize_append(
         _ptr(latent_bits), latent_bits.strides[0] // 2, _ptr(rope_bits), rope_bits.strides[0] // 2,
-        _ptr(slots), T, _ptr(cache), cache.shape[0], record_bytes))
+        _ptr(slots), T, _ptr(cache), cache.shape[0], record_bytes, _block_flag(record_bytes, block_scales)))
 
 
-def dequant_records(records: np.ndarray) -> np.ndarray:
+def dequant_records(records: np.ndarray, block_scales: bool = False) -> np.ndarray:
     """records uint8 [n, R] -> fp64 [n, 576] (K; V is K[:, :512])."""
     recs = _c(records, np.uint8)
     n, R = recs.shape
     out = np.empty((n, 576), dtype=np.float64)
-    lib().oracle_dequant_records(_ptr(recs), n, R, _ptr(out))
+    lib().oracle_dequant_records(_ptr(recs), n, R, _block_flag(R, block_scales), _ptr(out))
     return out
 
 
@@ -168,7 +178,7 @@ def dequant_records(records: np.ndarray) -> np.ndarray:
 
 def sparse_mla_decode(q_bits: np.ndarray, cache: np.ndarray, indices: np.ndarray, sm_scale: float,
                       attn_sink: Optional[np.ndarray] = None, rows: Optional[np.ndarray] = None,
-                      threads: int = 0) -> Tuple[np.ndarray, np.ndarray]:
+                      threads: int = 0, block_scales: bool = False) -> Tuple[np.ndarray, np.ndarray]:
     """q bf16 bits [n_tok, h_q, 576] (any leading shape flattened), cache uint8 [N, R],
     indices int32 [n_tok, topk]. Returns fp64 out [n_rows, h_q, 512] and lse [n_rows, h_q]
     for the query rows listed in ``rows`` (all rows when None)."""
@@ -185,7 +195,8 @@ def sparse_mla_decode(q_bits: np.ndarray, cache: np.ndarray, indices: np.ndarray
     n_rows = n_tok if tok is None else tok.size
     out = np.empty((n_rows, h_q, 512), dtype=np.float64)
     lse = np.empty((n_rows, h_q), dtype=np.float64)
-    lib().oracle_sparse_mla_decode(_ptr(q), _ptr(cache), cache.shape[0], cache.shape[1], _ptr(idx), topk,
+    lib().oracle_sparse_mla_decode(_ptr(q), _ptr(cache), cache.shape[0], cache.shape[1],
+                                   _block_flag(cache.shape[1], block_scales), _ptr(idx), topk,
                                    n_tok, h_q, topk, float(sm_scale), _ptr(sink), _ptr(tok),
                                    0 if tok is None else tok.size, _ptr(out), _ptr(lse), int(threads))
     return out, lse

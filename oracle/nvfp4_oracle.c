@@ -110,15 +110,19 @@ uint8_t oracle_e2m1_encode(float f) {
 
 /* Byte offset of the e4m3 scale of 16-element block g inside a record.
  * 352 B ([FlashMLA-18] layout): block s is stored at 320 + 8*(s & 3) + (s >> 2).
- * 432 B ([vLLM-82] Problem): 32 scale bytes in block order after the 256 NoPE bytes. */
-int oracle_scale_offset(int record_bytes, int g) {
-    if (record_bytes == 352) return 320 + 8 * (g & 3) + (g >> 2);
+ * 352 B with block_order != 0: the same 32-byte field holds the scales in block order (block s
+ *   at 320 + s). No page defines this record; it is the unpermuted side of the scale-layout
+ *   comparison that [FlashMLA-18] (layout) credits with 10-12% of decode latency.
+ * 432 B ([vLLM-82] Problem): 32 scale bytes in block order after the 256 NoPE bytes
+ *   (block_order is ignored). */
+int oracle_scale_offset(int record_bytes, int block_order, int g) {
+    if (record_bytes == 352) return block_order ? 320 + g : 320 + 8 * (g & 3) + (g >> 2);
     return 256 + g;
 }
 
 /* Quantize one token: 512 bf16 NoPE values and 64 bf16 RoPE values -> one record. */
 void oracle_quantize_record(const uint16_t* latent, const uint16_t* rope, int record_bytes,
-                            uint8_t* rec) {
+                            int block_order, uint8_t* rec) {
     uint8_t nib[512];
     for (int g = 0; g < 32; ++g) {
         /* scale = E4M3(group_amax / 6)  ([vLLM-82] Tests) */
@@ -130,7 +134,7 @@ void oracle_quantize_record(const uint16_t* latent, const uint16_t* rope, int re
         volatile float quotient = amax / 6.0f;
         uint8_t sbyte = oracle_e4m3_encode(quotient);
         float s = (float)oracle_e4m3_decode(sbyte);
-        rec[oracle_scale_offset(record_bytes, g)] = sbyte;
+        rec[oracle_scale_offset(record_bytes, block_order, g)] = sbyte;
         /* values round-to-nearest-even onto the e2m1 grid after division by the scale */
         for (int i = 0; i < 16; ++i) {
             float x = bf16_bits_to_float(latent[16 * g + i]);
@@ -162,7 +166,7 @@ void oracle_quantize_record(const uint16_t* latent, const uint16_t* rope, int re
 int64_t oracle_quantize_append(const uint16_t* latent, int64_t latent_row_stride,
                                const uint16_t* rope, int64_t rope_row_stride,
                                const int64_t* slot_mapping, int64_t T, uint8_t* cache,
-                               int64_t num_slots, int record_bytes) {
+                               int64_t num_slots, int record_bytes, int block_order) {
     int64_t out_of_range = 0;
     for (int64_t t = 0; t < T; ++t) {
         int64_t slot = slot_mapping[t];
@@ -172,18 +176,18 @@ int64_t oracle_quantize_append(const uint16_t* latent, int64_t latent_row_stride
             continue;
         }
         oracle_quantize_record(latent + t * latent_row_stride, rope + t * rope_row_stride,
-                               record_bytes, cache + slot * (int64_t)record_bytes);
+                               record_bytes, block_order, cache + slot * (int64_t)record_bytes);
     }
     return out_of_range;
 }
 
 /* Dequantize a record into the 576-dim key: K[0:512] = e2m1(code) * scale of its block,
  * K[512:576] = RoPE (e4m3 for 352 B, bf16 for 432 B). V is K[0:512]. */
-void oracle_dequant_record(const uint8_t* rec, int record_bytes, double* k) {
+void oracle_dequant_record(const uint8_t* rec, int record_bytes, int block_order, double* k) {
     for (int d = 0; d < 512; ++d) {
         uint8_t byte = rec[d / 2];
         uint8_t nibble = (d & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 15);
-        double s = oracle_e4m3_decode(rec[oracle_scale_offset(record_bytes, d / 16)]);
+        double s = oracle_e4m3_decode(rec[oracle_scale_offset(record_bytes, block_order, d / 16)]);
         k[d] = oracle_e2m1_decode(nibble) * s;
     }
     for (int j = 0; j < 64; ++j) {
@@ -196,8 +200,9 @@ void oracle_dequant_record(const uint8_t* rec, int record_bytes, double* k) {
     }
 }
 
-void oracle_dequant_records(const uint8_t* recs, int64_t n, int record_bytes, double* k) {
-    for (int64_t i = 0; i < n; ++i) oracle_dequant_record(recs + i * record_bytes, record_bytes, k + i * 576);
+void oracle_dequant_records(const uint8_t* recs, int64_t n, int record_bytes, int block_order, double* k) {
+    for (int64_t i = 0; i < n; ++i)
+        oracle_dequant_record(recs + i * record_bytes, record_bytes, block_order, k + i * 576);
 }
 
 /*
@@ -214,7 +219,7 @@ void oracle_dequant_records(const uint8_t* recs, int64_t n, int record_bytes, do
  * The keys of a row are dequantized once and reused by all of its heads.
  */
 void oracle_sparse_mla_decode(const uint16_t* q, const uint8_t* cache, int64_t num_slots,
-                              int record_bytes, const int32_t* indices, int64_t idx_row_stride,
+                              int record_bytes, int block_order, const int32_t* indices, int64_t idx_row_stride,
                               int64_t n_tok, int h_q, int topk, double sm_scale,
                               const float* sink, const int64_t* tok_list, int64_t n_list,
                               double* out, double* lse, int threads) {
@@ -232,7 +237,8 @@ void oracle_sparse_mla_decode(const uint16_t* q, const uint8_t* cache, int64_t n
         for (int j = 0; j < topk; ++j) {
             int64_t slot = row[j];
             if (slot < 0 || slot >= num_slots) continue;
-            oracle_dequant_record(cache + slot * (int64_t)record_bytes, record_bytes, keys + 576 * (size_t)n_used);
+            oracle_dequant_record(cache + slot * (int64_t)record_bytes, record_bytes, block_order,
+                                  keys + 576 * (size_t)n_used);
             ++n_used;
         }
 #ifdef _OPENMP
