@@ -17,6 +17,7 @@ on its own batch (query rows shard with no exchange), value = rows of all ranks 
 from __future__ import annotations
 
 import argparse
+import functools
 import hashlib
 import json
 import math
@@ -43,7 +44,7 @@ PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # capture (dram__bytes_read.sum + dram__bytes_write.sum), keyed by the hash of the decode code
 # (comments removed) it was taken with; reported as null once that code changes. The merge kernel that follows it
 # re-reads the partials, which are L2-resident outside ncu's cache flushing.
-NCU_TRAFFIC = {"6c8e364a7b73": 34214912 + 41728}
+NCU_TRAFFIC = {"8d23ffc281c3": 34213888 + 23296}
 
 
 def load_peaks():
@@ -628,6 +629,40 @@ def run_sweep(args):
                           "valid_index_fraction": valid / w.indices.numel(), "peaks": peak_src}), flush=True)
         del cache
         torch.cuda.empty_cache()
+    # scale-layout comparison (FlashMLA PR 18, format block: the permuted scale placement is
+    # credited with 10-12% of decode latency): the batch decode workload on two pools of the same
+    # contents, one with permuted scales and one with block-order scales, timed in alternating
+    # rounds in one process
+    w = synth.batch_decode(seed=0)
+    q, idx = w.q.to(dev), w.indices.to(dev)
+    out = torch.empty((w.B, w.s_q, w.h_q, 512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((w.B, w.s_q, w.h_q), dtype=torch.float32, device=dev)
+    ws = torch.empty(max(1, lib.workspace_size(w.B, w.s_q, w.h_q, w.topk, w.record_bytes, 0)), dtype=torch.uint8,
+                     device=dev)
+    pools = {False: fill_pool(lib.quantize_append, w.num_slots, 352, w.pool_seed, dev),
+             True: fill_pool(functools.partial(lib.quantize_append, block_scales=True), w.num_slots, 352,
+                             w.pool_seed, dev)}
+    times = {(blk, kind): [] for blk in pools for kind in ("warm", "cold")}
+    for rnd in range(6):
+        for blk in ((False, True) if rnd % 2 == 0 else (True, False)):
+            def call(c=pools[blk], b=blk):
+                lib.sparse_mla_decode(q, c, idx, w.sm_scale, out=out, lse=lse, workspace=ws, block_scales=b)
+
+            for _ in range(3):
+                call()
+            torch.cuda.synchronize()
+            times[(blk, "warm")].append(_time_calls(call, iters))
+            times[(blk, "cold")].append(_time_calls(call, iters, flush))
+    med = {k: float(np.median(v)) * 1e6 for k, v in times.items()}
+    print(json.dumps({"sweep": True, "workload": "scale_layout_decode_b32_sq1_h128_topk2048_R352",
+                      "kind": "decode_scale_layout",
+                      "us_per_call_warm": {"permuted": med[(False, "warm")], "block_order": med[(True, "warm")]},
+                      "us_per_call_cold": {"permuted": med[(False, "cold")], "block_order": med[(True, "cold")]},
+                      "block_order_over_permuted_cold": med[(True, "cold")] / med[(False, "cold")],
+                      "block_order_over_permuted_warm": med[(True, "warm")] / med[(False, "warm")],
+                      "rounds": 6, "calls_per_round": iters}), flush=True)
+    del pools
+    torch.cuda.empty_cache()
     # write path (quantize-append of 65,536 tokens into a 262,144-slot pool)
     ww = synth.write_path(seed=0)
     cache = torch.full((ww.num_slots, ww.record_bytes), ww.fill_byte, dtype=torch.uint8, device=dev)

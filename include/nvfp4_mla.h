@@ -61,6 +61,17 @@ typedef enum {
     NVFP4_MLA_ERR_WORKSPACE = 4      /* workspace missing, too small or misaligned        */
 } nvfp4_mla_status;
 
+/*
+ * Record layout. Every call's `record_bytes` is 352 or 432, or
+ * (352 | NVFP4_MLA_SCALES_BLOCK_ORDER): a 352-byte record equal to "nvfp4.fp8rope" except that its
+ * 32 scales are stored in block order, block s at byte 320 + s. No page defines that record; it
+ * is the unpermuted side of the scale-layout comparison (FlashMLA PR 18, format block, credits
+ * the permuted placement with 10-12% of decode latency). A cache is read with the value it was
+ * written with; its rows are (record_bytes & 0xFFFF) bytes wide. Any other value returns
+ * NVFP4_MLA_ERR_UNSUPPORTED.
+ */
+#define NVFP4_MLA_SCALES_BLOCK_ORDER 0x10000
+
 /* Bits the kernels OR into *dev_status. */
 #define NVFP4_MLA_DEV_SLOT_OUT_OF_RANGE 0x1u  /* quantize_append: slot >= num_slots (skipped) */
 #define NVFP4_MLA_DEV_INDEX_OUT_OF_RANGE 0x2u /* decode: index >= num_slots (masked)          */
@@ -76,9 +87,9 @@ typedef enum {
  *                      the token (padding); a slot >= num_slots is skipped and sets
  *                      NVFP4_MLA_DEV_SLOT_OUT_OF_RANGE. Slots should be distinct; if two tokens
  *                      share a slot, which record lands there is unspecified.
- *   cache              uint8 [num_slots, record_bytes], 16-byte aligned. Only the slots named
- *                      by slot_mapping are written; every other byte is left untouched.
- *   record_bytes       352 or 432.
+ *   cache              uint8 [num_slots, record_bytes & 0xFFFF], 16-byte aligned. Only the
+ *                      slots named by slot_mapping are written; every other byte is untouched.
+ *   record_bytes       352 or 432, or 352 | NVFP4_MLA_SCALES_BLOCK_ORDER (see above).
  *   dev_status         nullable device uint32 (see NVFP4_MLA_DEV_*).
  * num_tokens == 0 is valid and launches nothing.
  */
@@ -106,8 +117,8 @@ NVFP4_MLA_API int nvfp4_sparse_mla_decode_workspace_size(int32_t batch, int32_t 
  * Sparse MLA decode (read side).
  *   q            bf16 [batch, s_q, h_q, 576], contiguous, 16-byte aligned. Dims [0,512) are
  *                the NoPE (latent) part, [512,576) the RoPE part.
- *   cache        uint8 [num_slots, record_bytes], 16-byte aligned, as written by
- *                nvfp4_mla_quantize_append.
+ *   cache        uint8 [num_slots, record_bytes & 0xFFFF], 16-byte aligned, as written by
+ *                nvfp4_mla_quantize_append with the same record_bytes.
  *   indices      int32 [batch, s_q, topk], contiguous: the cache slots each query row attends.
  *                An entry < 0 is masked (padding); an entry >= num_slots is masked and sets
  *                NVFP4_MLA_DEV_INDEX_OUT_OF_RANGE. Repeated entries count once per occurrence.

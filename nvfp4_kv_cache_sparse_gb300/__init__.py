@@ -16,6 +16,9 @@ import torch
 from . import build as _build
 
 RECORD_BYTES = (352, 432)
+# OR-ed into record_bytes: a 352-byte record whose scales are stored in block order (the
+# unpermuted side of the scale-layout comparison); the cache is still [N, 352]
+SCALES_BLOCK_ORDER = 0x10000
 D_NOPE, D_ROPE, D_QK, D_V = 512, 64, 576, 512
 
 OK = 0
@@ -104,10 +107,17 @@ def _need(cond: bool, msg: str):
         raise ValueError(msg)
 
 
+def _record_code(cache: torch.Tensor, block_scales: bool) -> int:
+    _need(not block_scales or cache.shape[1] == 352, "block_scales applies to 352-byte records")
+    return cache.shape[1] | (SCALES_BLOCK_ORDER if block_scales else 0)
+
+
 def quantize_append(kv_latent: torch.Tensor, k_rope: torch.Tensor, slot_mapping: torch.Tensor,
-                    cache: torch.Tensor, dev_status: Optional[torch.Tensor] = None, stream=None) -> None:
+                    cache: torch.Tensor, dev_status: Optional[torch.Tensor] = None, stream=None,
+                    block_scales: bool = False) -> None:
     """Quantize ``kv_latent`` (bf16 [T,512]) and ``k_rope`` (bf16 [T,64]) into records and
-    write them to ``cache`` (uint8 [num_slots, 352|432]) at ``slot_mapping`` (int64 [T])."""
+    write them to ``cache`` (uint8 [num_slots, 352|432]) at ``slot_mapping`` (int64 [T]).
+    ``block_scales``: write 352-byte records with their scales in block order."""
     _need(kv_latent.dtype == torch.bfloat16 and k_rope.dtype == torch.bfloat16, "inputs must be bf16")
     _need(kv_latent.dim() == 2 and kv_latent.shape[1] == D_NOPE and kv_latent.stride(1) == 1, "kv_latent [T,512], inner stride 1")
     _need(k_rope.dim() == 2 and k_rope.shape[1] == D_ROPE and k_rope.stride(1) == 1, "k_rope [T,64], inner stride 1")
@@ -120,7 +130,7 @@ def quantize_append(kv_latent: torch.Tensor, k_rope: torch.Tensor, slot_mapping:
         _need(t.is_cuda and t.device == cache.device, "all tensors on the same CUDA device")
     st = load().nvfp4_mla_quantize_append(
         _ptr(kv_latent), kv_latent.stride(0), _ptr(k_rope), k_rope.stride(0), _ptr(slot_mapping), T,
-        _ptr(cache), cache.shape[0], cache.shape[1], _ptr(dev_status), _stream(stream))
+        _ptr(cache), cache.shape[0], _record_code(cache, block_scales), _ptr(dev_status), _stream(stream))
     _check("nvfp4_mla_quantize_append", st)
 
 
@@ -135,9 +145,10 @@ def sparse_mla_decode(q: torch.Tensor, cache: torch.Tensor, indices: torch.Tenso
                       attn_sink: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
                       lse: Optional[torch.Tensor] = None, num_splits: int = 0,
                       workspace: Optional[torch.Tensor] = None, dev_status: Optional[torch.Tensor] = None,
-                      stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+                      stream=None, block_scales: bool = False) -> Tuple[torch.Tensor, torch.Tensor]:
     """q bf16 [B, s_q, h_q, 576], cache uint8 [N, 352|432], indices int32 [B, s_q, topk].
-    Returns (out bf16 [B, s_q, h_q, 512], lse fp32 [B, s_q, h_q])."""
+    Returns (out bf16 [B, s_q, h_q, 512], lse fp32 [B, s_q, h_q]). ``block_scales``: the cache
+    holds 352-byte records with their scales in block order."""
     _need(q.dtype == torch.bfloat16 and q.dim() == 4 and q.shape[3] == D_QK and q.is_contiguous(), "q bf16 [B,s_q,h_q,576] contiguous")
     B, s_q, h_q, _ = q.shape
     _need(indices.dtype == torch.int32 and indices.dim() == 3 and tuple(indices.shape[:2]) == (B, s_q)
@@ -155,12 +166,13 @@ def sparse_mla_decode(q: torch.Tensor, cache: torch.Tensor, indices: torch.Tenso
     _need(lse.dtype == torch.float32 and lse.is_contiguous() and tuple(lse.shape) == (B, s_q, h_q), "lse fp32 [B,s_q,h_q]")
     for t in (q, cache, indices, out, lse) + ((attn_sink,) if attn_sink is not None else ()):
         _need(t.is_cuda and t.device == q.device, "all tensors on the same CUDA device")
-    need = workspace_size(B, s_q, h_q, topk, cache.shape[1], num_splits)
+    code = _record_code(cache, block_scales)
+    need = workspace_size(B, s_q, h_q, topk, code, num_splits)
     if need and (workspace is None or workspace.numel() * workspace.element_size() < need):
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     st = load().nvfp4_sparse_mla_decode(
-        _ptr(q), _ptr(cache), cache.shape[0], cache.shape[1], _ptr(indices), B, s_q, h_q, topk, float(sm_scale),
+        _ptr(q), _ptr(cache), cache.shape[0], code, _ptr(indices), B, s_q, h_q, topk, float(sm_scale),
         _ptr(attn_sink), _ptr(out), _ptr(lse), int(num_splits), _ptr(workspace), wbytes, _ptr(dev_status),
         _stream(stream))
     _check("nvfp4_sparse_mla_decode", st)

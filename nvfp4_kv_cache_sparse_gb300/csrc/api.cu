@@ -51,7 +51,10 @@ int device_sm_count(int* status) {
     return sms;
 }
 
-bool record_ok(int32_t r) { return r == 352 || r == 432; }
+// 352, 432, or 352 with its scales in block order (NVFP4_MLA_SCALES_BLOCK_ORDER)
+bool record_ok(int32_t r) { return r == 352 || r == 432 || r == (352 | NVFP4_MLA_SCALES_BLOCK_ORDER); }
+int record_width(int32_t r) { return r & 0xFFFF; }
+bool block_scales(int32_t r) { return (r & NVFP4_MLA_SCALES_BLOCK_ORDER) != 0; }
 
 // One CTA per (row, split, value half) and one CTA per SM: aim for one full wave.
 int auto_splits(int64_t rows, int32_t topk, int sm_count) {
@@ -102,7 +105,8 @@ NVFP4_MLA_API int nvfp4_mla_quantize_append(const void* kv_latent, int64_t laten
     const int sms = device_sm_count(&status);
     if (sms <= 0) return status;
     const cudaError_t e = nvfp4mla::launch_quantize_append(kv_latent, latent_row_stride, k_rope, rope_row_stride,
-                                                           slot_mapping, num_tokens, cache, num_slots, record_bytes,
+                                                           slot_mapping, num_tokens, cache, num_slots,
+                                                           record_width(record_bytes), block_scales(record_bytes),
                                                            dev_status, sms, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? NVFP4_MLA_OK : NVFP4_MLA_ERR_CUDA;
 }
@@ -149,7 +153,8 @@ NVFP4_MLA_API int nvfp4_sparse_mla_decode(const void* q, const uint8_t* cache, i
     d.q = q;
     d.cache = cache;
     d.num_slots = num_slots;
-    d.record_bytes = record_bytes;
+    d.record_bytes = record_width(record_bytes);
+    d.block_scales = block_scales(record_bytes);
     d.indices = indices;
     d.rows = static_cast<int>(rows);
     d.h_q = h_q;

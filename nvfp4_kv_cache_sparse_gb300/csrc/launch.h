@@ -10,14 +10,15 @@ namespace nvfp4mla {
 
 cudaError_t launch_quantize_append(const void* kv_latent, int64_t latent_row_stride, const void* k_rope,
                                    int64_t rope_row_stride, const int64_t* slot_mapping, int64_t num_tokens,
-                                   uint8_t* cache, int64_t num_slots, int record_bytes, uint32_t* dev_status,
-                                   int sm_count, cudaStream_t stream);
+                                   uint8_t* cache, int64_t num_slots, int record_bytes, bool block_scales,
+                                   uint32_t* dev_status, int sm_count, cudaStream_t stream);
 
 struct DecodeArgs {
     const void* q;             // bf16 [rows, h_q, 576]
     const uint8_t* cache;      // [num_slots, record_bytes]
     int64_t num_slots;
-    int record_bytes;
+    int record_bytes;          // 352 or 432
+    bool block_scales;         // 352 only: scales in block order instead of the permuted placement
     const int32_t* indices;    // [rows, topk]
     int rows;                  // batch * s_q
     int h_q;

@@ -4,7 +4,9 @@
 // Record formats:
 //  * 352 B, FlashMLA PR 18 "W4A16 DSA: NVFP4 KV cache format for SM100 sparse decode",
 //    format block "nvfp4.fp8rope (352 B/token)": [0,256) e2m1 pairs, [256,320) unscaled e4m3
-//    RoPE, [320,352) e4m3 scales with block s at byte 320 + 8*(s&3) + (s>>2).
+//    RoPE, [320,352) e4m3 scales with block s at byte 320 + 8*(s&3) + (s>>2). With kBlk the
+//    scales of a 352-byte record are stored in block order instead (block s at 320 + s), the
+//    unpermuted record of the scale-layout comparison in the same format block.
 //  * 432 B, vLLM PR 82 "kv: nvfp4_ds_mla - 4-bit NVFP4 KV cache for B12X sparse MLA (SM120)",
 //    Problem / Fix (Write side): [0,256) e2m1 pairs, [256,288) scales in block order,
 //    [288,304) zeros, [304,432) bf16 RoPE copied verbatim.
@@ -74,7 +76,7 @@ __device__ __forceinline__ float round_to_12_bits(float v) {
     return __uint_as_float((__float_as_uint(v) + 0x800u) & ~0xFFFu);
 }
 
-template <int R>
+template <int R, bool kBlk>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32, kBlocksPerSm)
 quantize_append_kernel(const uint16_t* __restrict__ latent, int64_t latent_stride, const uint16_t* __restrict__ rope,
                        int64_t rope_stride, const int64_t* __restrict__ slot_mapping, int64_t num_tokens,
@@ -139,7 +141,7 @@ quantize_append_kernel(const uint16_t* __restrict__ latent, int64_t latent_strid
 
             // ---- RoPE: lane owns elements 2*lane and 2*lane+1
             if constexpr (R == 352) {
-                rec[320 + 8 * (lane & 3) + (lane >> 2)] = static_cast<uint8_t>(sbyte);
+                rec[kBlk ? 320 + lane : 320 + 8 * (lane & 3) + (lane >> 2)] = static_cast<uint8_t>(sbyte);
                 uint32_t c = e4m3x2_rn_sat(fabsf(bf16_hi(rw[u])), fabsf(bf16_lo(rw[u])));
                 c |= ((rw[u] >> 8) & 0x80u) | ((rw[u] >> 16) & 0x8000u);
                 *reinterpret_cast<uint16_t*>(rec + 256 + 2 * lane) = static_cast<uint16_t>(c);
@@ -162,8 +164,8 @@ quantize_append_kernel(const uint16_t* __restrict__ latent, int64_t latent_strid
 
 cudaError_t launch_quantize_append(const void* kv_latent, int64_t latent_row_stride, const void* k_rope,
                                    int64_t rope_row_stride, const int64_t* slot_mapping, int64_t num_tokens,
-                                   uint8_t* cache, int64_t num_slots, int record_bytes, uint32_t* dev_status,
-                                   int sm_count, cudaStream_t stream) {
+                                   uint8_t* cache, int64_t num_slots, int record_bytes, bool block_scales,
+                                   uint32_t* dev_status, int sm_count, cudaStream_t stream) {
     const int64_t want = (num_tokens + kWarpsPerBlock - 1) / kWarpsPerBlock;
     const int64_t cap = static_cast<int64_t>(sm_count) * kBlocksPerSm;   // one wave of resident blocks
     const int grid = static_cast<int>(want < cap ? want : cap);
@@ -180,12 +182,11 @@ cudaError_t launch_quantize_append(const void* kv_latent, int64_t latent_row_str
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const cudaError_t err =
-        record_bytes == 352
-            ? cudaLaunchKernelEx(&cfg, quantize_append_kernel<352>, lat, latent_row_stride, rope, rope_row_stride,
-                                 slot_mapping, num_tokens, cache, num_slots, dev_status)
-            : cudaLaunchKernelEx(&cfg, quantize_append_kernel<432>, lat, latent_row_stride, rope, rope_row_stride,
-                                 slot_mapping, num_tokens, cache, num_slots, dev_status);
+    const auto kernel = record_bytes == 432 ? quantize_append_kernel<432, false>
+                        : block_scales      ? quantize_append_kernel<352, true>
+                                            : quantize_append_kernel<352, false>;
+    const cudaError_t err = cudaLaunchKernelEx(&cfg, kernel, lat, latent_row_stride, rope, rope_row_stride,
+                                               slot_mapping, num_tokens, cache, num_slots, dev_status);
     return err != cudaSuccess ? err : cudaGetLastError();
 }
 

@@ -270,9 +270,11 @@ __device__ __forceinline__ bool wait_warp(SmemCtl* ctl, uint64_t* bar, uint32_t 
 // Convert this thread's part of one key from its raw record in shared memory into the bf16
 // tile. Eight threads share a key: thread (q, hi) = (sub & 3, sub >> 2) converts the 16-wide NoPE
 // blocks 4c+q for c = 4hi..4hi+3 (their four scales are bytes 8q+4hi.. of the permuted scale field
-// of a 352-byte record: one 4-byte load) and RoPE dims [8 sub, 8 sub + 8). A masked key writes
-// zeros in a V tile and quiet NaNs in a K tile.
-template <int R, bool kRope>
+// of a 352-byte record: one 4-byte load; with the scales in block order, as in the 432-byte record
+// and the 352-byte record with kBlk, one 16-byte load of blocks 16hi..16hi+15 and a byte
+// selection) and RoPE dims [8 sub, 8 sub + 8). A masked key writes zeros in a V tile and quiet
+// NaNs in a K tile.
+template <int R, bool kRope, bool kBlk>
 __device__ __forceinline__ void convert_part(uint32_t rec, bool valid, uint32_t tile, int key, int sub) {
     const int q = sub & 3;
     const int hi = sub >> 2;
@@ -282,11 +284,11 @@ __device__ __forceinline__ void convert_part(uint32_t rec, bool valid, uint32_t 
 #pragma unroll
         for (int j = 0; j < 4; ++j) codes[j] = lds_u64(rec + 32 * (4 * hi + j) + 8 * q);
         uint32_t sw;   // four scale bytes, block 4(4hi + j) + q in byte j
-        if constexpr (R == 352) {
+        if constexpr (R == 352 && !kBlk) {
             sw = lds_u32(rec + 320 + 8 * q + 4 * hi);
         } else {
-            // natural order: block b at byte 256 + b
-            const uint4 s4 = lds_u128(rec + 256 + 16 * hi);
+            // block order: block b at byte 320 + b (352 B) or 256 + b (432 B)
+            const uint4 s4 = lds_u128(rec + (R == 352 ? 320 : 256) + 16 * hi);
             const uint32_t w[4] = {s4.x, s4.y, s4.z, s4.w};
             sw = 0u;
 #pragma unroll
@@ -390,7 +392,7 @@ __device__ __forceinline__ void produce_raw(const KernelArgs& a, SmemCtl* ctl, u
 // iteration. Waits for tile i's records in raw slot i % kRaw, converts them into stage
 // i % kStages of `ring` once the consumer released it (`empty`), arrives on `full` and hands the
 // raw slot back. With kRope (CTA 0) the K stages are written only after Q has left them (qready).
-template <int R, bool kRope, int kStages, int kStageBytes, int kRaw>
+template <int R, bool kRope, bool kBlk, int kStages, int kStageBytes, int kRaw>
 __device__ __forceinline__ void convert_tiles(const KernelArgs& a, SmemCtl* ctl, uint8_t* ring, uint8_t* raw,
                                               uint64_t* full, uint64_t* empty, int n_tiles, int t) {
     using RR = RawRing<R>;
@@ -406,7 +408,7 @@ __device__ __forceinline__ void convert_tiles(const KernelArgs& a, SmemCtl* ctl,
         if (i >= kStages && !wait_warp(ctl, &empty[ks], ((i - kStages) / kStages) & 1, a.status)) break;
         if (kRope && i == 0 && !wait_warp(ctl, &ctl->qready, 0, a.status)) break;   // K stages held Q
         const bool valid = ((ctl->rawvalid[rs][key >> 5] >> (key & 31)) & 1u) != 0u;
-        convert_part<R, kRope>(raw_s + rs * RR::kTileBytes + RR::key_offset(key), valid, ring_s + ks * kStageBytes,
+        convert_part<R, kRope, kBlk>(raw_s + rs * RR::kTileBytes + RR::key_offset(key), valid, ring_s + ks * kStageBytes,
                                key, sub);
         fence_proxy_async_smem();
         mbar_arrive(&full[ks]);
@@ -527,7 +529,7 @@ __device__ __forceinline__ void help_write_rows(const KernelArgs& a, const uint8
     }
 }
 
-template <int R>
+template <int R, bool kBlk>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) sparse_decode_kernel(const __grid_constant__ KernelArgs a) {
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte aligned base, computed as an offset into the shared array so that every access
@@ -752,7 +754,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) sparse_
             }
         } else if (converter) {
             // ============ CTA 0, warps 8-23: dequant of whole records (K tiles) ============
-            convert_tiles<R, true, kKStages, kKTileBytes, RawRing<R>::kStages0>(
+            convert_tiles<R, true, kBlk, kKStages, kKTileBytes, RawRing<R>::kStages0>(
                 a, ctl, smem + kOffK, smem + kOffRaw0, ctl->kfull, ctl->kempty, n_tiles, conv_t);
         } else if (warp >= kWarpProd) {
             // ============ CTA 0, warps 26-27: record gathers (TMA gather4) ============
@@ -855,7 +857,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) sparse_
             write_rows(smem, lane_base, have_o, factor, h, second ? 2 : 0);
         } else if (converter) {
             // ============ CTA 1, warps 8-23: dequant of the NoPE halves (V tiles) ============
-            convert_tiles<R, false, kVStages, kVTileBytes, RawRing<R>::kStages1>(
+            convert_tiles<R, false, kBlk, kVStages, kVTileBytes, RawRing<R>::kStages1>(
                 a, ctl, smem + kOffV, smem + kOffRaw1, ctl->vfull, ctl->vempty, n_tiles, conv_t);
             help_write_rows(a, smem, row, split, warp - kWarpConv0, lane);
         } else if (warp >= kWarpProd) {
@@ -1038,7 +1040,7 @@ bool encode_q_map(CUtensorMap* map, const void* q, int64_t heads) {
 }
 
 // Raises the kernel's dynamic shared memory limit once per device.
-template <int R>
+template <int R, bool kBlk>
 cudaError_t prepare_kernel() {
     static std::atomic<uint64_t> done{0};
     int dev = 0;
@@ -1046,7 +1048,8 @@ cudaError_t prepare_kernel() {
     if (err != cudaSuccess) return err;
     const uint64_t bit = dev < 64 ? (uint64_t(1) << dev) : 0;
     if (bit != 0 && (done.load(std::memory_order_relaxed) & bit)) return cudaSuccess;
-    err = cudaFuncSetAttribute(sparse_decode_kernel<R>, cudaFuncAttributeMaxDynamicSharedMemorySize, SmemSize<R>::value);
+    err = cudaFuncSetAttribute(sparse_decode_kernel<R, kBlk>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               SmemSize<R>::value);
     if (err == cudaSuccess && bit != 0) done.fetch_or(bit, std::memory_order_relaxed);
     return err;
 }
@@ -1079,7 +1082,9 @@ cudaError_t launch_sparse_decode(const DecodeArgs& d, cudaStream_t stream) {
     a.status = d.dev_status;
     const dim3 grid(static_cast<unsigned>(d.rows) * static_cast<unsigned>(d.splits) * 2u);
     const dim3 block(kThreads);
-    cudaError_t err = d.record_bytes == 352 ? prepare_kernel<352>() : prepare_kernel<432>();
+    cudaError_t err = d.record_bytes == 432 ? prepare_kernel<432, false>()
+                      : d.block_scales      ? prepare_kernel<352, true>()
+                                            : prepare_kernel<352, false>();
     if (err != cudaSuccess) return err;
     {
         cudaLaunchConfig_t cfg = {};
@@ -1092,8 +1097,10 @@ cudaError_t launch_sparse_decode(const DecodeArgs& d, cudaStream_t stream) {
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        err = d.record_bytes == 352 ? cudaLaunchKernelEx(&cfg, sparse_decode_kernel<352>, a)
-                                    : cudaLaunchKernelEx(&cfg, sparse_decode_kernel<432>, a);
+        const auto kernel = d.record_bytes == 432 ? sparse_decode_kernel<432, false>
+                            : d.block_scales      ? sparse_decode_kernel<352, true>
+                                                  : sparse_decode_kernel<352, false>;
+        err = cudaLaunchKernelEx(&cfg, kernel, a);
     }
     if (err == cudaSuccess) err = cudaGetLastError();
     if (err != cudaSuccess || d.splits == 1) return err;

@@ -29,6 +29,12 @@ def test_header_declares_the_expected_calls():
     assert set(syms) == set(lib.EXPORTED), syms
 
 
+def test_binding_constants_match_the_header():
+    text = open(HEADER).read()
+    m = re.search(r"#define NVFP4_MLA_SCALES_BLOCK_ORDER (0x[0-9a-fA-F]+)", text)
+    assert m and int(m.group(1), 16) == lib.SCALES_BLOCK_ORDER
+
+
 def test_library_exports_every_declared_symbol(cdll):
     for name in declared_symbols():
         assert hasattr(cdll, name), name
@@ -59,6 +65,14 @@ def test_host_side_checks_return_codes_without_a_device(cdll):
     assert cdll.nvfp4_mla_quantize_append(None, 512, None, 64, None, 0, None, 0, 352, None, None) == lib.OK
     assert cdll.nvfp4_mla_quantize_append(None, 512, None, 64, None, 4, None, 8, 352, None, None) == lib.ERR_INVALID_ARG
     assert cdll.nvfp4_mla_quantize_append(None, 512, None, 64, None, 4, None, 8, 353, None, None) == lib.ERR_UNSUPPORTED
+    # the block-order scale layout exists for the 352-byte record only
+    blk = lib.SCALES_BLOCK_ORDER
+    assert cdll.nvfp4_sparse_mla_decode_workspace_size(2, 1, 64, 64, 352 | blk, 2, ctypes.byref(n)) == lib.OK
+    assert n.value == 2 * 2 * 64 * 512 * 2 + 1024
+    for bad in (432 | blk, 352 | 0x20000, blk):
+        assert cdll.nvfp4_sparse_mla_decode_workspace_size(2, 1, 64, 64, bad, 2, ctypes.byref(n)) == lib.ERR_UNSUPPORTED
+        assert cdll.nvfp4_mla_quantize_append(None, 512, None, 64, None, 4, None, 8, bad, None, None) == lib.ERR_UNSUPPORTED
+    assert cdll.nvfp4_mla_quantize_append(None, 512, None, 64, None, 4, None, 8, 352 | blk, None, None) == lib.ERR_INVALID_ARG
     # decode: null pointers
     assert cdll.nvfp4_sparse_mla_decode(None, None, 8, 352, None, 1, 1, 64, 64, 1.0, None, None, None, 1, None, 0,
                                         None, None) == lib.ERR_INVALID_ARG
