@@ -23,7 +23,7 @@ _BUILD = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD, "liboracle.so")
 _lib = None
 
-RECORD_BYTES = (352, 432)
+RECORD_BYTES = (352, 432, 656)
 
 
 def build(force: bool = False) -> str:
@@ -57,6 +57,8 @@ def lib() -> ctypes.CDLL:
         _lib.oracle_e4m3_encode.argtypes = [ctypes.c_float]
         _lib.oracle_e2m1_encode.restype = ctypes.c_uint8
         _lib.oracle_e2m1_encode.argtypes = [ctypes.c_float]
+        _lib.oracle_round_to_bf16.restype = d
+        _lib.oracle_round_to_bf16.argtypes = [d]
         _lib.oracle_scale_offset.restype = i32
         _lib.oracle_scale_offset.argtypes = [i32, i32, i32]
         _lib.oracle_quantize_record.restype = None
@@ -124,9 +126,16 @@ def _block_flag(record_bytes: int, block_scales: bool) -> int:
     return 1 if block_scales else 0
 
 
+def round_to_bf16(x: float) -> float:
+    """Nearest bf16 value of a finite double, ties to even."""
+    return float(lib().oracle_round_to_bf16(float(x)))
+
+
 def scale_offset(record_bytes: int, g: int, block_scales: bool = False) -> int:
-    """Byte offset of block g's scale. ``block_scales``: the 352-byte record with its scales in
-    block order (the unpermuted side of the scale-layout comparison)."""
+    """Byte offset of 16-value block g's e4m3 scale in an NVFP4 record. ``block_scales``: the
+    352-byte record with its scales in block order (the unpermuted side of the scale-layout
+    comparison)."""
+    assert record_bytes in (352, 432)
     return int(lib().oracle_scale_offset(int(record_bytes), _block_flag(record_bytes, block_scales), int(g)))
 
 

@@ -18,7 +18,9 @@
  *                (vLLM fork pull request 82): "Problem" (the 432-B record field list),
  *                "Fix / Write side" (E2M1 data + per-16-group E4M3 scales, implicit global
  *                scale 1.0, zeroed pad, verbatim 16-bit RoPE) and "Tests" (scale =
- *                E4M3(group_amax/6), the E2M1 nibble table).
+ *                E4M3(group_amax/6), the E2M1 nibble table); the same "Problem" section
+ *                gives the 656-B fp8_ds_mla record (512 B fp8 NoPE + 16 B fp32 tile scales +
+ *                128 B bf16 RoPE) that the NVFP4 records are measured against.
  *
  * Readings of points the pages leave open:
  *  - e4m3 is the "fn" variant: no infinities, 0x7F/0xFF are NaN, largest finite 448.
@@ -31,6 +33,14 @@
  *  - The even element of a pair sits in the low nibble of its byte.
  *  - 432-B record: NoPE at 0, scales in group order at 256, 16 zero bytes at 288, bf16 RoPE
  *    (little-endian) at 304.
+ *  - 656-B record: the fields in the order the page lists them: 512 e4m3 NoPE codes at 0, four
+ *    little-endian fp32 scales at 512 (scale t covers NoPE values [128t, 128t+128)), 64 bf16
+ *    RoPE values (little-endian) at 528. No page states the fp8 scale rule; the one used is
+ *    the plain analogue of the NVFP4 rule: scale = amax / 448 (IEEE fp32 division, 448 = the
+ *    largest e4m3 magnitude) and code = e4m3(x / scale) (fp32 quotient); a tile whose amax is 0
+ *    stores scale 0 and zero codes carrying the input signs. Its dequantized key is rounded to
+ *    bf16 ("the kernel dequantizes to bf16", [FlashMLA-18]): K = bf16(e4m3(code) * scale),
+ *    one round-to-nearest-even of the exact product.
  *  - Decode: an index i is used iff 0 <= i < num_slots; repeated indices count as often as
  *    they appear. The log-sum-exp is natural-log, over the scaled logits of the used
  *    tokens only; an attention sink adds exp(sink - m) to the softmax denominator of `out`
@@ -55,6 +65,21 @@ static float bf16_bits_to_float(uint16_t bits) {
 }
 
 double oracle_bf16_to_double(uint16_t bits) { return (double)bf16_bits_to_float(bits); }
+
+/* Round a finite double to the nearest bf16 value (8 significant bits, the fp32 exponent
+ * range, subnormals in steps of 2^-133), ties to even; beyond the largest bf16 value it
+ * overflows to infinity. Used for the fp8 record's keys. */
+double oracle_round_to_bf16(double x) {
+    if (x == 0.0 || !isfinite(x)) return x;
+    int e;
+    (void)frexp(x, &e);                         /* |x| = m * 2^e, m in [0.5, 1) */
+    int lsb = e - 8;                            /* weight of the last kept bit */
+    if (lsb < -133) lsb = -133;                 /* bf16 subnormal spacing */
+    double q = ldexp(x, -lsb);                  /* exact: a power-of-two scaling */
+    double r = ldexp(nearbyint(q), lsb);        /* default rounding mode: ties to even */
+    /* past the largest bf16 value (just below 2^128) the nearest is infinity */
+    return fabs(r) >= ldexp(1.0, 128) ? copysign(INFINITY, x) : r;
+}
 
 /* e4m3 (fn) decode by its bit fields: sign, 4 exponent bits (bias 7), 3 mantissa bits. */
 double oracle_e4m3_decode(uint8_t code) {
@@ -121,8 +146,39 @@ int oracle_scale_offset(int record_bytes, int block_order, int g) {
 }
 
 /* Quantize one token: 512 bf16 NoPE values and 64 bf16 RoPE values -> one record. */
+/* The 656-B fp8 record: per 128-value tile t, scale = amax / 448 and code = e4m3(x / scale). */
+static void quantize_record_fp8(const uint16_t* latent, const uint16_t* rope, uint8_t* rec) {
+    for (int t = 0; t < 4; ++t) {
+        float amax = 0.0f;
+        for (int i = 0; i < 128; ++i) {
+            float a = fabsf(bf16_bits_to_float(latent[128 * t + i]));
+            if (a > amax) amax = a;
+        }
+        volatile float scale = amax / 448.0f;
+        float s = scale;
+        memcpy(rec + 512 + 4 * t, &s, 4);       /* little-endian fp32 on every host this runs on */
+        for (int i = 0; i < 128; ++i) {
+            float x = bf16_bits_to_float(latent[128 * t + i]);
+            if (s == 0.0f) {
+                rec[128 * t + i] = signbit(x) ? 0x80 : 0x00;
+            } else {
+                volatile float v = x / s;
+                rec[128 * t + i] = oracle_e4m3_encode(v);
+            }
+        }
+    }
+    for (int j = 0; j < 64; ++j) {
+        rec[528 + 2 * j] = (uint8_t)(rope[j] & 0xFF);
+        rec[529 + 2 * j] = (uint8_t)(rope[j] >> 8);
+    }
+}
+
 void oracle_quantize_record(const uint16_t* latent, const uint16_t* rope, int record_bytes,
                             int block_order, uint8_t* rec) {
+    if (record_bytes == 656) {
+        quantize_record_fp8(latent, rope, rec);
+        return;
+    }
     uint8_t nib[512];
     for (int g = 0; g < 32; ++g) {
         /* scale = E4M3(group_amax / 6)  ([vLLM-82] Tests) */
@@ -184,6 +240,19 @@ int64_t oracle_quantize_append(const uint16_t* latent, int64_t latent_row_stride
 /* Dequantize a record into the 576-dim key: K[0:512] = e2m1(code) * scale of its block,
  * K[512:576] = RoPE (e4m3 for 352 B, bf16 for 432 B). V is K[0:512]. */
 void oracle_dequant_record(const uint8_t* rec, int record_bytes, int block_order, double* k) {
+    if (record_bytes == 656) {
+        /* K[0:512] = bf16(e4m3(code) * scale of its tile), K[512:576] = bf16 RoPE */
+        for (int d = 0; d < 512; ++d) {
+            float s;
+            memcpy(&s, rec + 512 + 4 * (d / 128), 4);
+            k[d] = oracle_round_to_bf16(oracle_e4m3_decode(rec[d]) * (double)s);
+        }
+        for (int j = 0; j < 64; ++j) {
+            uint16_t bits = (uint16_t)(rec[528 + 2 * j] | (rec[529 + 2 * j] << 8));
+            k[512 + j] = oracle_bf16_to_double(bits);
+        }
+        return;
+    }
     for (int d = 0; d < 512; ++d) {
         uint8_t byte = rec[d / 2];
         uint8_t nibble = (d & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 15);
