@@ -17,6 +17,7 @@ on its own batch (query rows shard with no exchange), value = rows of all ranks 
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import functools
 import hashlib
 import json
@@ -600,7 +601,10 @@ def run_sweep(args):
                    ("decode_b32_sq1_h128_topk2048_R352", synth.batch_decode(seed=0)),
                    ("varlen_b128_sq2_h64_topk2048_R352_sink", synth.varlen_decode(seed=0)),
                    ("longctx_b64_sq1_h128_topk2048_R432", synth.long_context(seed=0)),
-                   ("prefill_b2_sq256_h128_topk2048_prefix16384_R352", synth.sparse_prefill(seed=0))]
+                   ("prefill_b2_sq256_h128_topk2048_prefix16384_R352", synth.sparse_prefill(seed=0)),
+                   # the same batch decode over 656-byte fp8 records (the NVFP4-vs-fp8 comparison)
+                   ("decode_b32_sq1_h128_topk2048_R656",
+                    dataclasses.replace(synth.batch_decode(seed=0), record_bytes=656))]
     for name, w in decode_cfgs:
         cache = fill_pool(lib.quantize_append, w.num_slots, w.record_bytes, w.pool_seed, dev)
         q, idx = w.q.to(dev), w.indices.to(dev)

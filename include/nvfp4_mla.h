@@ -14,6 +14,14 @@
  *       scales in block order, 16 zero bytes, 128 B bf16 RoPE copied verbatim.
  *     - Scale rule (vLLM PR 82, Tests): scale = E4M3(group_amax / 6); values are rounded to
  *       the nearest e2m1 grid point after division by the decoded scale.
+ *     - 656-byte fp8 record, the one the NVFP4 records are measured against (vLLM PR 82,
+ *       Problem: "512 B fp8 NoPE + 16 B fp32 tile scales + 128 B BF16 RoPE"): bytes [0,512)
+ *       e4m3 NoPE codes, [512,528) four little-endian fp32 scales (scale t covers NoPE values
+ *       [128t, 128t+128)), [528,656) bf16 RoPE copied verbatim. The page gives no fp8 scale
+ *       rule; this library uses scale = amax / 448 and code = e4m3(x / scale) (fp32 quotients;
+ *       a zero tile stores scale 0), and the decode's keys are bf16(e4m3 * scale). The decode
+ *       takes V in f16, so NoPE magnitudes must stay below 65536 (the append flags larger
+ *       ones with NVFP4_MLA_DEV_FP8_RANGE and stores them anyway).
  *
  *  2. nvfp4_sparse_mla_decode: DeepSeek-style sparse MLA decode over one shared latent KV
  *     head: for each query row (b, i) and head h, the keys are the records its top-k index
@@ -62,7 +70,7 @@ typedef enum {
 } nvfp4_mla_status;
 
 /*
- * Record layout. Every call's `record_bytes` is 352 or 432, or
+ * Record layout. Every call's `record_bytes` is 352, 432 or 656, or
  * (352 | NVFP4_MLA_SCALES_BLOCK_ORDER): a 352-byte record equal to "nvfp4.fp8rope" except that its
  * 32 scales are stored in block order, block s at byte 320 + s. No page defines that record; it
  * is the unpermuted side of the scale-layout comparison (FlashMLA PR 18, format block, credits
@@ -76,6 +84,7 @@ typedef enum {
 #define NVFP4_MLA_DEV_SLOT_OUT_OF_RANGE 0x1u  /* quantize_append: slot >= num_slots (skipped) */
 #define NVFP4_MLA_DEV_INDEX_OUT_OF_RANGE 0x2u /* decode: index >= num_slots (masked)          */
 #define NVFP4_MLA_DEV_TIMEOUT 0x4u            /* decode: a pipeline wait gave up; out invalid */
+#define NVFP4_MLA_DEV_FP8_RANGE 0x8u          /* quantize_append, 656 B: a NoPE |x| >= 65536  */
 
 /*
  * Quantize-and-append (write side).
@@ -89,7 +98,7 @@ typedef enum {
  *                      share a slot, which record lands there is unspecified.
  *   cache              uint8 [num_slots, record_bytes & 0xFFFF], 16-byte aligned. Only the
  *                      slots named by slot_mapping are written; every other byte is untouched.
- *   record_bytes       352 or 432, or 352 | NVFP4_MLA_SCALES_BLOCK_ORDER (see above).
+ *   record_bytes       352, 432 or 656, or 352 | NVFP4_MLA_SCALES_BLOCK_ORDER (see above).
  *   dev_status         nullable device uint32 (see NVFP4_MLA_DEV_*).
  * num_tokens == 0 is valid and launches nothing.
  */
@@ -135,7 +144,8 @@ NVFP4_MLA_API int nvfp4_sparse_mla_decode_workspace_size(int32_t batch, int32_t 
  *                arguments, 256-byte aligned; may be NULL when that size is 0. Its contents
  *                need no initialization.
  *   dev_status   nullable device uint32 (see NVFP4_MLA_DEV_*).
- * Precision: dequantized keys are exact (bf16 for QK^T, f16 for PV); the two contractions
+ * Precision: dequantized NVFP4 keys are exact (bf16 for QK^T, f16 for PV); fp8 keys are
+ * e4m3 * scale rounded in fp32 and then to bf16 (QK^T) or f16 (PV); the two contractions
  * run on tcgen05 16-bit MMAs with fp32 accumulation (P enters PV as f16); softmax in fp32;
  * `out` is rounded to bf16 once, after the parts' f16 partial outputs (relative error
  * <= 2^-11 each) are merged in fp32 when the top-k list is split.

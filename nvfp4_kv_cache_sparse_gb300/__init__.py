@@ -15,7 +15,7 @@ import torch
 
 from . import build as _build
 
-RECORD_BYTES = (352, 432)
+RECORD_BYTES = (352, 432, 656)
 # OR-ed into record_bytes: a 352-byte record whose scales are stored in block order (the
 # unpermuted side of the scale-layout comparison); the cache is still [N, 352]
 SCALES_BLOCK_ORDER = 0x10000
@@ -29,6 +29,7 @@ ERR_WORKSPACE = 4
 DEV_SLOT_OUT_OF_RANGE = 0x1
 DEV_INDEX_OUT_OF_RANGE = 0x2
 DEV_TIMEOUT = 0x4
+DEV_FP8_RANGE = 0x8
 
 EXPORTED = (
     "nvfp4_mla_quantize_append",
@@ -116,7 +117,7 @@ def quantize_append(kv_latent: torch.Tensor, k_rope: torch.Tensor, slot_mapping:
                     cache: torch.Tensor, dev_status: Optional[torch.Tensor] = None, stream=None,
                     block_scales: bool = False) -> None:
     """Quantize ``kv_latent`` (bf16 [T,512]) and ``k_rope`` (bf16 [T,64]) into records and
-    write them to ``cache`` (uint8 [num_slots, 352|432]) at ``slot_mapping`` (int64 [T]).
+    write them to ``cache`` (uint8 [num_slots, 352|432|656]) at ``slot_mapping`` (int64 [T]).
     ``block_scales``: write 352-byte records with their scales in block order."""
     _need(kv_latent.dtype == torch.bfloat16 and k_rope.dtype == torch.bfloat16, "inputs must be bf16")
     _need(kv_latent.dim() == 2 and kv_latent.shape[1] == D_NOPE and kv_latent.stride(1) == 1, "kv_latent [T,512], inner stride 1")
@@ -125,7 +126,7 @@ def quantize_append(kv_latent: torch.Tensor, k_rope: torch.Tensor, slot_mapping:
     _need(k_rope.shape[0] == T and slot_mapping.numel() == T, "token counts differ")
     _need(slot_mapping.dtype == torch.int64 and slot_mapping.is_contiguous(), "slot_mapping int64 contiguous")
     _need(cache.dtype == torch.uint8 and cache.dim() == 2 and cache.is_contiguous(), "cache uint8 [num_slots, R] contiguous")
-    _need(cache.shape[1] in RECORD_BYTES, "record width must be 352 or 432")
+    _need(cache.shape[1] in RECORD_BYTES, "record width must be 352, 432 or 656")
     for t in (kv_latent, k_rope, slot_mapping, cache):
         _need(t.is_cuda and t.device == cache.device, "all tensors on the same CUDA device")
     st = load().nvfp4_mla_quantize_append(
@@ -146,7 +147,7 @@ def sparse_mla_decode(q: torch.Tensor, cache: torch.Tensor, indices: torch.Tenso
                       lse: Optional[torch.Tensor] = None, num_splits: int = 0,
                       workspace: Optional[torch.Tensor] = None, dev_status: Optional[torch.Tensor] = None,
                       stream=None, block_scales: bool = False) -> Tuple[torch.Tensor, torch.Tensor]:
-    """q bf16 [B, s_q, h_q, 576], cache uint8 [N, 352|432], indices int32 [B, s_q, topk].
+    """q bf16 [B, s_q, h_q, 576], cache uint8 [N, 352|432|656], indices int32 [B, s_q, topk].
     Returns (out bf16 [B, s_q, h_q, 512], lse fp32 [B, s_q, h_q]). ``block_scales``: the cache
     holds 352-byte records with their scales in block order."""
     _need(q.dtype == torch.bfloat16 and q.dim() == 4 and q.shape[3] == D_QK and q.is_contiguous(), "q bf16 [B,s_q,h_q,576] contiguous")
@@ -155,7 +156,7 @@ def sparse_mla_decode(q: torch.Tensor, cache: torch.Tensor, indices: torch.Tenso
           and indices.is_contiguous(), "indices int32 [B,s_q,topk] contiguous")
     topk = indices.shape[2]
     _need(cache.dtype == torch.uint8 and cache.dim() == 2 and cache.is_contiguous() and cache.shape[1] in RECORD_BYTES,
-          "cache uint8 [N, 352|432] contiguous")
+          "cache uint8 [N, 352|432|656] contiguous")
     if attn_sink is not None:
         _need(attn_sink.dtype == torch.float32 and attn_sink.numel() == h_q and attn_sink.is_contiguous(), "attn_sink fp32 [h_q]")
     if out is None:

@@ -51,8 +51,10 @@ int device_sm_count(int* status) {
     return sms;
 }
 
-// 352, 432, or 352 with its scales in block order (NVFP4_MLA_SCALES_BLOCK_ORDER)
-bool record_ok(int32_t r) { return r == 352 || r == 432 || r == (352 | NVFP4_MLA_SCALES_BLOCK_ORDER); }
+// 352, 432, 656 (fp8), or 352 with its scales in block order (NVFP4_MLA_SCALES_BLOCK_ORDER)
+bool record_ok(int32_t r) {
+    return r == 352 || r == 432 || r == 656 || r == (352 | NVFP4_MLA_SCALES_BLOCK_ORDER);
+}
 int record_width(int32_t r) { return r & 0xFFFF; }
 bool block_scales(int32_t r) { return (r & NVFP4_MLA_SCALES_BLOCK_ORDER) != 0; }
 

@@ -10,6 +10,11 @@
 //  * 432 B, vLLM PR 82 "kv: nvfp4_ds_mla - 4-bit NVFP4 KV cache for B12X sparse MLA (SM120)",
 //    Problem / Fix (Write side): [0,256) e2m1 pairs, [256,288) scales in block order,
 //    [288,304) zeros, [304,432) bf16 RoPE copied verbatim.
+//  * 656 B, the fp8 record the same vLLM page (Problem) measures against: [0,512) e4m3 NoPE,
+//    [512,528) four fp32 scales (one per 128 values), [528,656) bf16 RoPE copied verbatim.
+//    The page states no fp8 scale rule; this kernel uses scale = amax / 448 per 128-value tile
+//    and code = e4m3(x / scale), both IEEE fp32 divisions (a zero tile stores scale 0 and
+//    signed zero codes).
 // Scale rule (vLLM PR 82, Tests): scale = E4M3(group_amax / 6), round-to-nearest-even and
 // saturating; each value is rounded to the nearest e2m1 grid point (ties to even, saturating)
 // after division by the decoded scale; the sign of the input is always kept.
@@ -17,7 +22,8 @@
 // Design: one warp per token, lane g owns the 16-value group g. The group maximum is taken on
 // the |bf16| bit patterns (non-negative floats order like integers), so no shuffles are
 // needed. The record is assembled in a per-warp shared-memory stage and written with 16-byte
-// stores (22 lanes for 352 B, 27 for 432 B), so each record is one contiguous burst.
+// stores (22 lanes for 352 B, 27 for 432 B, 41 chunks over 32 lanes for 656 B), so each record
+// is one contiguous burst.
 //
 // Exactness of x / s without a division per value: s is an e4m3 value (<= 4 significant bits)
 // and x a bf16 value (<= 8), so the exact quotient x/s is either exactly one of the e2m1 tie
@@ -124,6 +130,27 @@ quantize_append_kernel(const uint16_t* __restrict__ latent, int64_t latent_strid
             uint32_t amax_bits = 0;
 #pragma unroll
             for (int k = 0; k < 8; ++k) amax_bits = max(amax_bits, max(w[k] & 0x7FFFu, (w[k] >> 16) & 0x7FFFu));
+            if constexpr (R == 656) {
+                // ---- fp8 record: the 8 lanes of a 128-value tile share its maximum
+                amax_bits = max(amax_bits, __shfl_xor_sync(0xffffffffu, amax_bits, 1));
+                amax_bits = max(amax_bits, __shfl_xor_sync(0xffffffffu, amax_bits, 2));
+                amax_bits = max(amax_bits, __shfl_xor_sync(0xffffffffu, amax_bits, 4));
+                const float scale = __fdiv_rn(__uint_as_float(amax_bits << 16), 448.0f);
+                // |x| >= 65536 is stored, but lies beyond the f16 value operand of the decode
+                if ((lane & 7) == 0 && amax_bits >= 0x4780u && dev_status != nullptr) atomicOr(dev_status, 0x8u);
+                uint32_t packed[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const float q0 = scale != 0.0f ? __fdiv_rn(fabsf(bf16_lo(w[k])), scale) : 0.0f;
+                    const float q1 = scale != 0.0f ? __fdiv_rn(fabsf(bf16_hi(w[k])), scale) : 0.0f;
+                    uint32_t c = e4m3x2_rn_sat(q1, q0);                       // byte 2k: element 2k
+                    c |= ((w[k] >> 8) & 0x80u) | ((w[k] >> 16) & 0x8000u);   // signs of both elements
+                    packed[k >> 1] |= c << (16 * (k & 1));
+                }
+                *reinterpret_cast<uint4*>(rec + 16 * lane) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+                if ((lane & 7) == 0) *reinterpret_cast<float*>(rec + 512 + 4 * (lane >> 3)) = scale;
+                *reinterpret_cast<uint32_t*>(rec + 528 + 4 * lane) = rw[u];
+            } else {
             const float amax = __uint_as_float(amax_bits << 16);
             const uint32_t sbyte = e4m3x2_rn_sat(0.0f, __fdiv_rn(amax, 6.0f)) & 0xFFu;
             const float inv_s = sbyte ? __frcp_rn(e4m3_code_value(sbyte)) : 0.0f;
@@ -150,10 +177,11 @@ quantize_append_kernel(const uint16_t* __restrict__ latent, int64_t latent_strid
                 *reinterpret_cast<uint32_t*>(rec + 304 + 4 * lane) = rw[u];
                 if (lane < 4) *reinterpret_cast<uint32_t*>(rec + 288 + 4 * lane) = 0u;
             }
+            }
             __syncwarp();
-            if (lane < R / 16) {
-                const uint4 v = reinterpret_cast<const uint4*>(rec)[lane];
-                reinterpret_cast<uint4*>(cache + slot[u] * R)[lane] = v;
+            for (int c = lane; c < R / 16; c += 32) {
+                const uint4 v = reinterpret_cast<const uint4*>(rec)[c];
+                reinterpret_cast<uint4*>(cache + slot[u] * R)[c] = v;
             }
             __syncwarp();
         }
@@ -182,7 +210,8 @@ cudaError_t launch_quantize_append(const void* kv_latent, int64_t latent_row_str
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const auto kernel = record_bytes == 432 ? quantize_append_kernel<432, false>
+    const auto kernel = record_bytes == 656 ? quantize_append_kernel<656, false>
+                        : record_bytes == 432 ? quantize_append_kernel<432, false>
                         : block_scales      ? quantize_append_kernel<352, true>
                                             : quantize_append_kernel<352, false>;
     const cudaError_t err = cudaLaunchKernelEx(&cfg, kernel, lat, latent_row_stride, rope, rope_row_stride,

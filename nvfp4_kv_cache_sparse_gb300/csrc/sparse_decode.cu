@@ -24,7 +24,8 @@
 // Warp roles (kThreads = 896 threads, 28 warps):
 //   both:  warps 8-23 convert (8 threads per key of a 64-key tile), warps 26-27 gather
 //          records with TMA tile::gather4 into a ring of raw tiles (CTA 0: three for 352-B
-//          records, two for 432-B; CTA 1: two) and publish the used-key bits of each
+//          records, two for 432-B, one for 656-B; CTA 1: two, one for 656-B) and publish the
+//          used-key bits of each
 //          tile; warp 24 owns tensor memory.
 //   CTA 0: warps 0-7 softmax (warp w: TMEM lanes 32 (w & 3).., score columns 32 (w >> 2)..+32;
 //          the two column halves exchange tile maxima), warps 24-25 QK issuers (even / odd
@@ -63,13 +64,14 @@ constexpr int kPStages = 2;                        // CTA 1: P tiles [128 heads 
 constexpr int kPBytes = kHeadsM * 128;             // 16 KB
 // Raw-record ring, filled by TMA tile::gather4 (four whole records per instruction, each group of
 // four starting on a 128-byte boundary): CTA 0 keeps 3 tiles in flight for 352-byte records and
-// 2 for 432-byte records, CTA 1 keeps 2.
+// 2 for 432-byte records, CTA 1 keeps 2. A 64-key tile of 656-byte fp8 records takes 42 KB, so
+// each CTA holds one; its converters hand the slot back as soon as the bytes are in registers.
 template <int R>
 struct RawRing {
-    static constexpr int kGroupBytes = (4 * R + 127) / 128 * 128;   // 1408 | 1792
+    static constexpr int kGroupBytes = (4 * R + 127) / 128 * 128;   // 1408 | 1792 | 2688
     static constexpr int kTileBytes = 16 * kGroupBytes;             // 64 keys
-    static constexpr int kStages0 = R == 352 ? 3 : 2;
-    static constexpr int kStages1 = 2;
+    static constexpr int kStages0 = R == 352 ? 3 : R == 432 ? 2 : 1;
+    static constexpr int kStages1 = R == 656 ? 1 : 2;
     static __device__ __forceinline__ int key_offset(int key) { return (key >> 2) * kGroupBytes + (key & 3) * R; }
 };
 constexpr int kProducerWarps = 2;
@@ -135,7 +137,8 @@ struct SmemSize {
     static constexpr int c1 = kOffRaw1 + RawRing<R>::kStages1 * RawRing<R>::kTileBytes;
     static constexpr int value = 1024 + (c0 > c1 ? c0 : c1);
 };
-static_assert(SmemSize<352>::value <= 232448 && SmemSize<432>::value <= 232448, "shared memory");
+static_assert(SmemSize<352>::value <= 232448 && SmemSize<432>::value <= 232448 && SmemSize<656>::value <= 232448,
+              "shared memory");
 static_assert(kOffRaw0 % 128 == 0 && kOffRaw1 % 128 == 0, "gather4 destinations are 128-byte aligned");
 
 struct KernelArgs {
@@ -242,6 +245,32 @@ __device__ __forceinline__ void dq_block(uint2 codes, uint32_t sbyte, uint4& lo,
     hi.y = dq_pair<kF16>((codes.y >> 8) & 0xFFu, s2);
     hi.z = dq_pair<kF16>((codes.y >> 16) & 0xFFu, s2);
     hi.w = dq_pair<kF16>(codes.y >> 24, s2);
+}
+
+// Two e4m3 codes (low byte = even element) of a 656-byte fp8 record times its fp32 tile scale:
+// each product is formed in fp32 (round to nearest) and rounded once more to bf16 (kF16 false,
+// the QK operand) or f16 (kF16 true, the PV operand; NoPE magnitudes up to 65504).
+template <bool kF16>
+__device__ __forceinline__ uint32_t dq_e4m3x2_scaled(uint32_t two_bytes, float scale) {
+    uint32_t h;
+    const uint16_t in = static_cast<uint16_t>(two_bytes);
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(in));
+    const float2 f = __half22float2(*reinterpret_cast<__half2*>(&h));
+    const float a = __fmul_rn(f.x, scale), b = __fmul_rn(f.y, scale);
+    return kF16 ? pack_f16x2(a, b) : pack_bf16x2(a, b);
+}
+
+// 16 e4m3 values (16 bytes) of one 16-wide block -> 2 x 16 bytes of bf16 (or f16).
+template <bool kF16>
+__device__ __forceinline__ void dq_block_fp8(uint4 codes, float scale, uint4& lo, uint4& hi) {
+    lo.x = dq_e4m3x2_scaled<kF16>(codes.x, scale);
+    lo.y = dq_e4m3x2_scaled<kF16>(codes.x >> 16, scale);
+    lo.z = dq_e4m3x2_scaled<kF16>(codes.y, scale);
+    lo.w = dq_e4m3x2_scaled<kF16>(codes.y >> 16, scale);
+    hi.x = dq_e4m3x2_scaled<kF16>(codes.z, scale);
+    hi.y = dq_e4m3x2_scaled<kF16>(codes.z >> 16, scale);
+    hi.z = dq_e4m3x2_scaled<kF16>(codes.w, scale);
+    hi.w = dq_e4m3x2_scaled<kF16>(codes.w >> 16, scale);
 }
 
 __device__ __forceinline__ void set_abort(SmemCtl* ctl, uint32_t* status) {
@@ -414,6 +443,69 @@ __device__ __forceinline__ void convert_tiles(const KernelArgs& a, SmemCtl* ctl,
         mbar_arrive(&full[ks]);
         __syncwarp();
         if (lane == 0) mbar_arrive(&ctl->rawempty[rs]);
+    }
+}
+
+// Converter warps for 656-byte fp8 records (one raw slot per CTA). Thread (q, hi) = (sub & 3,
+// sub >> 2) of key `key` converts NoPE dims 64c + 16q .. +15 for c = 4hi..4hi+3 (codes at byte
+// 64c + 16q, fp32 scales of tiles 2hi and 2hi + 1 at byte 512 + 8hi) and, in a K tile, RoPE dims
+// [8 sub, 8 sub + 8) (bf16 at byte 528 + 16 sub). All of a tile's record bytes are loaded into
+// registers first; then the warp hands the raw slot back (so the next gather overlaps the
+// conversion), waits for the ring stage, converts and stores. Masked keys as in convert_part.
+template <bool kRope, int kStages, int kStageBytes>
+__device__ __forceinline__ void convert_tiles_fp8(const KernelArgs& a, SmemCtl* ctl, uint8_t* ring, uint8_t* raw,
+                                                  uint64_t* full, uint64_t* empty, int n_tiles, int t) {
+    using RR = RawRing<656>;
+    const int key = t >> 3;
+    const int sub = t & 7;
+    const int lane = t & 31;
+    const int q = sub & 3;
+    const int hi = sub >> 2;
+    const uint32_t rec = smem_addr(raw) + RR::key_offset(key);
+    const uint32_t ring_s = smem_addr(ring);
+    for (int i = 0; i < n_tiles; ++i) {
+        const int ks = i % kStages;
+        if (!wait_warp(ctl, &ctl->rawfull[0], i & 1, a.status)) break;
+        const bool valid = ((ctl->rawvalid[0][key >> 5] >> (key & 31)) & 1u) != 0u;
+        uint4 codes[4];
+        uint2 sc = make_uint2(0u, 0u);
+        uint4 rope = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) codes[j] = make_uint4(0u, 0u, 0u, 0u);
+        if (valid) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) codes[j] = lds_u128(rec + 64 * (4 * hi + j) + 16 * q);
+            sc = lds_u64(rec + 512 + 8 * hi);
+            if constexpr (kRope) rope = lds_u128(rec + 528 + 16 * sub);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl->rawempty[0]);
+        if (i >= kStages && !wait_warp(ctl, &empty[ks], ((i - kStages) / kStages) & 1, a.status)) break;
+        if (kRope && i == 0 && !wait_warp(ctl, &ctl->qready, 0, a.status)) break;   // K stages held Q
+        const uint32_t tile = ring_s + ks * kStageBytes;
+        if (valid) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int c = 4 * hi + j;
+                uint4 lo, hv;
+                dq_block_fp8<!kRope>(codes[j], __uint_as_float(j < 2 ? sc.x : sc.y), lo, hv);
+                sts_u128(tile + c * kBlkBytes + swz(key, 2 * q), lo);
+                sts_u128(tile + c * kBlkBytes + swz(key, 2 * q + 1), hv);
+            }
+            if constexpr (kRope) sts_u128(tile + 8 * kBlkBytes + swz(key, sub), rope);
+        } else {
+            const uint32_t f = kRope ? 0x7FC07FC0u : 0u;
+            const uint4 z = make_uint4(f, f, f, f);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int c = 4 * hi + j;
+                sts_u128(tile + c * kBlkBytes + swz(key, 2 * q), z);
+                sts_u128(tile + c * kBlkBytes + swz(key, 2 * q + 1), z);
+            }
+            if constexpr (kRope) sts_u128(tile + 8 * kBlkBytes + swz(key, sub), z);
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(&full[ks]);
     }
 }
 
@@ -754,8 +846,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) sparse_
             }
         } else if (converter) {
             // ============ CTA 0, warps 8-23: dequant of whole records (K tiles) ============
-            convert_tiles<R, true, kBlk, kKStages, kKTileBytes, RawRing<R>::kStages0>(
-                a, ctl, smem + kOffK, smem + kOffRaw0, ctl->kfull, ctl->kempty, n_tiles, conv_t);
+            if constexpr (R == 656)
+                convert_tiles_fp8<true, kKStages, kKTileBytes>(a, ctl, smem + kOffK, smem + kOffRaw0, ctl->kfull,
+                                                               ctl->kempty, n_tiles, conv_t);
+            else
+                convert_tiles<R, true, kBlk, kKStages, kKTileBytes, RawRing<R>::kStages0>(
+                    a, ctl, smem + kOffK, smem + kOffRaw0, ctl->kfull, ctl->kempty, n_tiles, conv_t);
         } else if (warp >= kWarpProd) {
             // ============ CTA 0, warps 26-27: record gathers (TMA gather4) ============
             produce_raw<R, true, RawRing<R>::kStages0>(a, ctl, smem + kOffRaw0, idx_row, key_begin, key_end, n_tiles,
@@ -857,8 +953,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) sparse_
             write_rows(smem, lane_base, have_o, factor, h, second ? 2 : 0);
         } else if (converter) {
             // ============ CTA 1, warps 8-23: dequant of the NoPE halves (V tiles) ============
-            convert_tiles<R, false, kBlk, kVStages, kVTileBytes, RawRing<R>::kStages1>(
-                a, ctl, smem + kOffV, smem + kOffRaw1, ctl->vfull, ctl->vempty, n_tiles, conv_t);
+            if constexpr (R == 656)
+                convert_tiles_fp8<false, kVStages, kVTileBytes>(a, ctl, smem + kOffV, smem + kOffRaw1, ctl->vfull,
+                                                                ctl->vempty, n_tiles, conv_t);
+            else
+                convert_tiles<R, false, kBlk, kVStages, kVTileBytes, RawRing<R>::kStages1>(
+                    a, ctl, smem + kOffV, smem + kOffRaw1, ctl->vfull, ctl->vempty, n_tiles, conv_t);
             help_write_rows(a, smem, row, split, warp - kWarpConv0, lane);
         } else if (warp >= kWarpProd) {
             // ============ CTA 1, warps 26-27: record gathers (TMA gather4) ============
@@ -1082,7 +1182,8 @@ cudaError_t launch_sparse_decode(const DecodeArgs& d, cudaStream_t stream) {
     a.status = d.dev_status;
     const dim3 grid(static_cast<unsigned>(d.rows) * static_cast<unsigned>(d.splits) * 2u);
     const dim3 block(kThreads);
-    cudaError_t err = d.record_bytes == 432 ? prepare_kernel<432, false>()
+    cudaError_t err = d.record_bytes == 656 ? prepare_kernel<656, false>()
+                      : d.record_bytes == 432 ? prepare_kernel<432, false>()
                       : d.block_scales      ? prepare_kernel<352, true>()
                                             : prepare_kernel<352, false>();
     if (err != cudaSuccess) return err;
@@ -1090,14 +1191,17 @@ cudaError_t launch_sparse_decode(const DecodeArgs& d, cudaStream_t stream) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = grid;
         cfg.blockDim = block;
-        cfg.dynamicSmemBytes = d.record_bytes == 352 ? SmemSize<352>::value : SmemSize<432>::value;
+        cfg.dynamicSmemBytes = d.record_bytes == 656   ? SmemSize<656>::value
+                               : d.record_bytes == 432 ? SmemSize<432>::value
+                                                       : SmemSize<352>::value;
         cfg.stream = stream;
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // see griddepcontrol.wait
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        const auto kernel = d.record_bytes == 432 ? sparse_decode_kernel<432, false>
+        const auto kernel = d.record_bytes == 656 ? sparse_decode_kernel<656, false>
+                            : d.record_bytes == 432 ? sparse_decode_kernel<432, false>
                             : d.block_scales      ? sparse_decode_kernel<352, true>
                                                   : sparse_decode_kernel<352, false>;
         err = cudaLaunchKernelEx(&cfg, kernel, a);

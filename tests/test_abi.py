@@ -65,11 +65,14 @@ def test_host_side_checks_return_codes_without_a_device(cdll):
     assert cdll.nvfp4_mla_quantize_append(None, 512, None, 64, None, 0, None, 0, 352, None, None) == lib.OK
     assert cdll.nvfp4_mla_quantize_append(None, 512, None, 64, None, 4, None, 8, 352, None, None) == lib.ERR_INVALID_ARG
     assert cdll.nvfp4_mla_quantize_append(None, 512, None, 64, None, 4, None, 8, 353, None, None) == lib.ERR_UNSUPPORTED
+    # the 656-byte fp8 record
+    assert cdll.nvfp4_sparse_mla_decode_workspace_size(2, 1, 64, 64, 656, 2, ctypes.byref(n)) == lib.OK
+    assert cdll.nvfp4_mla_quantize_append(None, 512, None, 64, None, 4, None, 8, 656, None, None) == lib.ERR_INVALID_ARG
     # the block-order scale layout exists for the 352-byte record only
     blk = lib.SCALES_BLOCK_ORDER
     assert cdll.nvfp4_sparse_mla_decode_workspace_size(2, 1, 64, 64, 352 | blk, 2, ctypes.byref(n)) == lib.OK
     assert n.value == 2 * 2 * 64 * 512 * 2 + 1024
-    for bad in (432 | blk, 352 | 0x20000, blk):
+    for bad in (432 | blk, 656 | blk, 352 | 0x20000, blk):
         assert cdll.nvfp4_sparse_mla_decode_workspace_size(2, 1, 64, 64, bad, 2, ctypes.byref(n)) == lib.ERR_UNSUPPORTED
         assert cdll.nvfp4_mla_quantize_append(None, 512, None, 64, None, 4, None, 8, bad, None, None) == lib.ERR_UNSUPPORTED
     assert cdll.nvfp4_mla_quantize_append(None, 512, None, 64, None, 4, None, 8, 352 | blk, None, None) == lib.ERR_INVALID_ARG
