@@ -45,7 +45,7 @@ PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # capture (dram__bytes_read.sum + dram__bytes_write.sum), keyed by the hash of the decode code
 # (comments removed) it was taken with; reported as null once that code changes. The merge kernel that follows it
 # re-reads the partials, which are L2-resident outside ncu's cache flushing.
-NCU_TRAFFIC = {"8d23ffc281c3": 34213888 + 23296}
+NCU_TRAFFIC = {"77755f3d8009": 34213376 + 29184}
 
 
 def load_peaks():
@@ -667,26 +667,30 @@ def run_sweep(args):
                       "rounds": 6, "calls_per_round": iters}), flush=True)
     del pools
     torch.cuda.empty_cache()
-    # write path (quantize-append of 65,536 tokens into a 262,144-slot pool)
-    ww = synth.write_path(seed=0)
-    cache = torch.full((ww.num_slots, ww.record_bytes), ww.fill_byte, dtype=torch.uint8, device=dev)
-    lat, rope, slots = ww.latent.to(dev), ww.rope.to(dev), ww.slot_mapping.to(dev)
+    # write path (quantize-append of 65,536 tokens into a 262,144-slot pool), 352-byte records and
+    # the 656-byte fp8 records they are compared with
+    for R in (352, 656):
+        ww = synth.write_path(seed=0, record_bytes=R)
+        cache = torch.full((ww.num_slots, ww.record_bytes), ww.fill_byte, dtype=torch.uint8, device=dev)
+        lat, rope, slots = ww.latent.to(dev), ww.rope.to(dev), ww.slot_mapping.to(dev)
 
-    def append():
-        lib.quantize_append(lat, rope, slots, cache)
+        def append():
+            lib.quantize_append(lat, rope, slots, cache)
 
-    for _ in range(3):
-        append()
-    torch.cuda.synchronize()
-    warm = _time_calls(append, iters)
-    cold = _time_calls(append, iters, flush)
-    bytes_ = ww.T * (512 * 2 + 64 * 2 + 8 + ww.record_bytes)
-    t_roof = bytes_ / (hbm * 1e9)
-    print(json.dumps({"sweep": True, "workload": ww.name, "kind": "quantize_append", "tokens": ww.T,
-                      "us_per_call_warm": warm * 1e6, "us_per_call_cold": cold * 1e6,
-                      "tokens_per_s_cold": ww.T / cold, "achieved_gbs_cold": bytes_ / cold / 1e9,
-                      "roofline_us": t_roof * 1e6, "roofline_frac_cold": t_roof / cold, "bound": "hbm",
-                      "algorithmic_bytes": bytes_, "peaks": peak_src}), flush=True)
+        for _ in range(3):
+            append()
+        torch.cuda.synchronize()
+        warm = _time_calls(append, iters)
+        cold = _time_calls(append, iters, flush)
+        bytes_ = ww.T * (512 * 2 + 64 * 2 + 8 + ww.record_bytes)
+        t_roof = bytes_ / (hbm * 1e9)
+        print(json.dumps({"sweep": True, "workload": ww.name, "kind": "quantize_append", "tokens": ww.T,
+                          "us_per_call_warm": warm * 1e6, "us_per_call_cold": cold * 1e6,
+                          "tokens_per_s_cold": ww.T / cold, "achieved_gbs_cold": bytes_ / cold / 1e9,
+                          "roofline_us": t_roof * 1e6, "roofline_frac_cold": t_roof / cold, "bound": "hbm",
+                          "algorithmic_bytes": bytes_, "peaks": peak_src}), flush=True)
+        del cache
+        torch.cuda.empty_cache()
 
 
 def main():
