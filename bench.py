@@ -605,7 +605,10 @@ def run_sweep(args):
                    # the same batch decode over 656-byte fp8 records (the NVFP4-vs-fp8 comparison)
                    ("decode_b32_sq1_h128_topk2048_R656",
                     dataclasses.replace(synth.batch_decode(seed=0), record_bytes=656))]
+    want = lambda name: args.sweep_filter is None or args.sweep_filter in name   # noqa: E731
     for name, w in decode_cfgs:
+        if not want(name):
+            continue
         cache = fill_pool(lib.quantize_append, w.num_slots, w.record_bytes, w.pool_seed, dev)
         q, idx = w.q.to(dev), w.indices.to(dev)
         sink = None if w.attn_sink is None else w.attn_sink.to(dev)
@@ -637,6 +640,20 @@ def run_sweep(args):
     # credited with 10-12% of decode latency): the batch decode workload on two pools of the same
     # contents, one with permuted scales and one with block-order scales, timed in alternating
     # rounds in one process
+    if want("scale_layout_decode_b32_sq1_h128_topk2048_R352"):
+        run_scale_layout(args, dev, iters, flush)
+    # write path (quantize-append of 65,536 tokens into a 262,144-slot pool), 352-byte records and
+    # the 656-byte fp8 records they are compared with
+    for R in (352, 656):
+        ww = synth.write_path(seed=0, record_bytes=R)
+        if not want(ww.name):
+            continue
+        run_write(ww, dev, iters, flush, hbm, peak_src)
+
+
+def run_scale_layout(args, dev, iters, flush):
+    import nvfp4_kv_cache_sparse_gb300 as lib
+    from synth.pool import fill_pool
     w = synth.batch_decode(seed=0)
     q, idx = w.q.to(dev), w.indices.to(dev)
     out = torch.empty((w.B, w.s_q, w.h_q, 512), dtype=torch.bfloat16, device=dev)
@@ -667,30 +684,30 @@ def run_sweep(args):
                       "rounds": 6, "calls_per_round": iters}), flush=True)
     del pools
     torch.cuda.empty_cache()
-    # write path (quantize-append of 65,536 tokens into a 262,144-slot pool), 352-byte records and
-    # the 656-byte fp8 records they are compared with
-    for R in (352, 656):
-        ww = synth.write_path(seed=0, record_bytes=R)
-        cache = torch.full((ww.num_slots, ww.record_bytes), ww.fill_byte, dtype=torch.uint8, device=dev)
-        lat, rope, slots = ww.latent.to(dev), ww.rope.to(dev), ww.slot_mapping.to(dev)
 
-        def append():
-            lib.quantize_append(lat, rope, slots, cache)
 
-        for _ in range(3):
-            append()
-        torch.cuda.synchronize()
-        warm = _time_calls(append, iters)
-        cold = _time_calls(append, iters, flush)
-        bytes_ = ww.T * (512 * 2 + 64 * 2 + 8 + ww.record_bytes)
-        t_roof = bytes_ / (hbm * 1e9)
-        print(json.dumps({"sweep": True, "workload": ww.name, "kind": "quantize_append", "tokens": ww.T,
-                          "us_per_call_warm": warm * 1e6, "us_per_call_cold": cold * 1e6,
-                          "tokens_per_s_cold": ww.T / cold, "achieved_gbs_cold": bytes_ / cold / 1e9,
-                          "roofline_us": t_roof * 1e6, "roofline_frac_cold": t_roof / cold, "bound": "hbm",
-                          "algorithmic_bytes": bytes_, "peaks": peak_src}), flush=True)
-        del cache
-        torch.cuda.empty_cache()
+def run_write(ww, dev, iters, flush, hbm, peak_src):
+    import nvfp4_kv_cache_sparse_gb300 as lib
+    cache = torch.full((ww.num_slots, ww.record_bytes), ww.fill_byte, dtype=torch.uint8, device=dev)
+    lat, rope, slots = ww.latent.to(dev), ww.rope.to(dev), ww.slot_mapping.to(dev)
+
+    def append():
+        lib.quantize_append(lat, rope, slots, cache)
+
+    for _ in range(3):
+        append()
+    torch.cuda.synchronize()
+    warm = _time_calls(append, iters)
+    cold = _time_calls(append, iters, flush)
+    bytes_ = ww.T * (512 * 2 + 64 * 2 + 8 + ww.record_bytes)
+    t_roof = bytes_ / (hbm * 1e9)
+    print(json.dumps({"sweep": True, "workload": ww.name, "kind": "quantize_append", "tokens": ww.T,
+                      "us_per_call_warm": warm * 1e6, "us_per_call_cold": cold * 1e6,
+                      "tokens_per_s_cold": ww.T / cold, "achieved_gbs_cold": bytes_ / cold / 1e9,
+                      "roofline_us": t_roof * 1e6, "roofline_frac_cold": t_roof / cold, "bound": "hbm",
+                      "algorithmic_bytes": bytes_, "peaks": peak_src}), flush=True)
+    del cache
+    torch.cuda.empty_cache()
 
 
 def main():
@@ -705,6 +722,8 @@ def main():
     ap.add_argument("--sweep", action="store_true",
                     help="time every workload configuration (decode and write path), one JSON line each")
     ap.add_argument("--sweep-iters", type=int, default=20)
+    ap.add_argument("--sweep-filter", default=None,
+                    help="with --sweep: time only the configurations whose name contains this string")
     args = ap.parse_args()
     if args.sweep:
         run_sweep(args)
