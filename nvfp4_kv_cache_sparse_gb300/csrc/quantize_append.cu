@@ -20,10 +20,10 @@
 // after division by the decoded scale; the sign of the input is always kept.
 //
 // Design: one warp per token, lane g owns the 16-value group g. The group maximum is taken on
-// the |bf16| bit patterns (non-negative floats order like integers), so no shuffles are
-// needed. The record is assembled in a per-warp shared-memory stage and written with 16-byte
-// stores (22 lanes for 352 B, 27 for 432 B, 41 chunks over 32 lanes for 656 B), so each record
-// is one contiguous burst.
+// the |bf16| bit patterns (non-negative floats order like integers) with packed 16-bit maxima,
+// so no shuffles are needed. The record is assembled in a per-warp shared-memory stage and
+// written with 16-byte stores (22 lanes for 352 B, 27 for 432 B, 41 chunks over 32 lanes for
+// 656 B), so each record is one contiguous burst.
 //
 // Exactness of x / s without a division per value: s is an e4m3 value (<= 4 significant bits)
 // and x a bf16 value (<= 8), so the exact quotient x/s is either exactly one of the e2m1 tie
@@ -31,7 +31,15 @@
 // them. q = |x| * rn(1/s) is within 2^-23 (relative) of x/s; rounding q to 12 significant bits
 // therefore lands exactly on the tie point in the first case and cannot cross one in the
 // second, so the hardware e2m1 rounding of that value equals the rounding of the IEEE
-// quotient. amax / 6 uses a correctly rounded division (one per group).
+// quotient. The same holds for q keeping the sign of x (the rounding acts on the magnitude
+// bits), and the hardware conversions keep the sign, so a negative value that rounds to zero
+// gives the negative-zero code.
+//
+// amax / 6 as amax * rn(1/6): amax has at most 8 significant bits. If amax / 6 is an e4m3 tie
+// point T (at most 5 significant bits), the product is T (1 + d) with |d| <= 2^-24, which rounds
+// to T in fp32; otherwise amax / 6 lies at least 2^-10.6 (relative) from every tie point, far
+// beyond the product's error. Either way the e4m3 rounding equals that of amax / 6. Per block,
+// rn(1/s) of every e4m3 scale is kept in a shared table.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -77,9 +85,24 @@ __device__ __forceinline__ float e4m3_code_value(uint32_t c) {
     return e ? __uint_as_float(((e + 120u) << 23) | (m << 20)) : static_cast<float>(m) * 0.001953125f;
 }
 
-// Round a non-negative float to 12 significant bits (see the file comment).
+// Round a float's magnitude to 12 significant bits, half away from zero (see the file comment).
 __device__ __forceinline__ float round_to_12_bits(float v) {
     return __uint_as_float((__float_as_uint(v) + 0x800u) & ~0xFFFu);
+}
+
+// Per-halfword unsigned maximum of two packed pairs.
+__device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("max.u16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+// e4m3 codes of two floats (signs kept), round-to-nearest-even, saturating:
+// bits [15:8] = code(hi), [7:0] = code(lo).
+__device__ __forceinline__ uint32_t e4m3x2_signed(float hi, float lo) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
 }
 
 template <int R, bool kBlk>
@@ -88,10 +111,15 @@ quantize_append_kernel(const uint16_t* __restrict__ latent, int64_t latent_strid
                        int64_t rope_stride, const int64_t* __restrict__ slot_mapping, int64_t num_tokens,
                        uint8_t* __restrict__ cache, int64_t num_slots, uint32_t* __restrict__ dev_status) {
     __shared__ __align__(16) uint8_t stage[kWarpsPerBlock][R];
+    __shared__ float inv_scale[128];   // rn(1 / value) of each e4m3 scale code; 0 for code 0
     // A decode launched next on the stream may start its prologue now; it waits for this grid
     // before it reads anything. This grid is itself a programmatic dependent of the preceding
-    // kernel and waits for it to complete before reading or writing memory.
+    // kernel and waits for it to complete before reading or writing memory (the table needs
+    // neither).
     asm volatile("griddepcontrol.launch_dependents;");
+    if (R != 656 && threadIdx.x < 128)
+        inv_scale[threadIdx.x] = threadIdx.x ? __frcp_rn(e4m3_code_value(threadIdx.x)) : 0.0f;
+    __syncthreads();
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -127,9 +155,13 @@ quantize_append_kernel(const uint16_t* __restrict__ latent, int64_t latent_strid
             }
             // ---- NoPE group `lane`: 16 bf16 values
             const uint32_t w[8] = {va[u].x, va[u].y, va[u].z, va[u].w, vb[u].x, vb[u].y, vb[u].z, vb[u].w};
-            uint32_t amax_bits = 0;
-#pragma unroll
-            for (int k = 0; k < 8; ++k) amax_bits = max(amax_bits, max(w[k] & 0x7FFFu, (w[k] >> 16) & 0x7FFFu));
+            // group maximum on |bf16| bit patterns (non-negative floats order like integers), two
+            // per 32-bit word
+            uint32_t m2 = max_u16x2(max_u16x2(max_u16x2(w[0] & 0x7FFF7FFFu, w[1] & 0x7FFF7FFFu),
+                                              max_u16x2(w[2] & 0x7FFF7FFFu, w[3] & 0x7FFF7FFFu)),
+                                    max_u16x2(max_u16x2(w[4] & 0x7FFF7FFFu, w[5] & 0x7FFF7FFFu),
+                                              max_u16x2(w[6] & 0x7FFF7FFFu, w[7] & 0x7FFF7FFFu)));
+            uint32_t amax_bits = max(m2 & 0xFFFFu, m2 >> 16);
             if constexpr (R == 656) {
                 // ---- fp8 record: the 8 lanes of a 128-value tile share its maximum
                 amax_bits = max(amax_bits, __shfl_xor_sync(0xffffffffu, amax_bits, 1));
@@ -152,25 +184,26 @@ quantize_append_kernel(const uint16_t* __restrict__ latent, int64_t latent_strid
                 *reinterpret_cast<uint32_t*>(rec + 528 + 4 * lane) = rw[u];
             } else {
             const float amax = __uint_as_float(amax_bits << 16);
-            const uint32_t sbyte = e4m3x2_rn_sat(0.0f, __fdiv_rn(amax, 6.0f)) & 0xFFu;
-            const float inv_s = sbyte ? __frcp_rn(e4m3_code_value(sbyte)) : 0.0f;
+            const uint32_t sbyte = e4m3x2_rn_sat(0.0f, amax * (1.0f / 6.0f)) & 0xFFu;
+            const float inv_s = inv_scale[sbyte];
 
             uint32_t packed[2] = {0u, 0u};
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
-                const float q0 = round_to_12_bits(fabsf(bf16_lo(w[k])) * inv_s);
-                const float q1 = round_to_12_bits(fabsf(bf16_hi(w[k])) * inv_s);
-                uint32_t byte = e2m1x2_rn_sat(q1, q0);                    // even element -> low nibble
-                byte |= ((w[k] >> 12) & 0x8u) | ((w[k] >> 24) & 0x80u);   // signs of both elements
-                packed[k >> 2] |= byte << (8 * (k & 3));
+                const float q0 = round_to_12_bits(bf16_lo(w[k]) * inv_s);
+                const float q1 = round_to_12_bits(bf16_hi(w[k]) * inv_s);
+                const uint32_t byte = e2m1x2_rn_sat(q1, q0);              // even element -> low nibble
+                packed[k >> 2] = (k & 3) ? __byte_perm(packed[k >> 2], byte, (k & 3) == 1 ? 0x3240u
+                                                                            : (k & 3) == 2 ? 0x3410u
+                                                                                           : 0x4210u)
+                                         : byte;
             }
             *reinterpret_cast<uint2*>(rec + 8 * lane) = make_uint2(packed[0], packed[1]);
 
             // ---- RoPE: lane owns elements 2*lane and 2*lane+1
             if constexpr (R == 352) {
                 rec[kBlk ? 320 + lane : 320 + 8 * (lane & 3) + (lane >> 2)] = static_cast<uint8_t>(sbyte);
-                uint32_t c = e4m3x2_rn_sat(fabsf(bf16_hi(rw[u])), fabsf(bf16_lo(rw[u])));
-                c |= ((rw[u] >> 8) & 0x80u) | ((rw[u] >> 16) & 0x8000u);
+                const uint32_t c = e4m3x2_signed(bf16_hi(rw[u]), bf16_lo(rw[u]));
                 *reinterpret_cast<uint16_t*>(rec + 256 + 2 * lane) = static_cast<uint16_t>(c);
             } else {
                 rec[256 + lane] = static_cast<uint8_t>(sbyte);
