@@ -51,7 +51,7 @@ namespace nvfp4mla {
 namespace {
 
 constexpr int kWarpsPerBlock = 8;
-constexpr int kTokensPerRound = 4;
+constexpr int kTokensPerRound = 2;
 constexpr int kBlocksPerSm = 4;
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
@@ -125,27 +125,39 @@ quantize_append_kernel(const uint16_t* __restrict__ latent, int64_t latent_strid
     const int lane = threadIdx.x & 31;
     uint8_t* rec = stage[warp];
 
-    // kTokensPerRound tokens per warp per round: all their loads (slot, 32 latent bytes and 4
-    // RoPE bytes per lane) are issued before any of them is converted, so their memory latencies
-    // overlap.
+    // kTokensPerRound tokens per warp per round. The loads of a round (slot, 32 latent bytes and
+    // 4 RoPE bytes per lane per token) are issued before the previous round is converted, so a
+    // warp always has a round in flight while it converts.
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kWarpsPerBlock;
-    for (int64_t t0 = static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + warp; t0 < num_tokens;
-         t0 += stride * kTokensPerRound) {
+    struct Round {
         int64_t slot[kTokensPerRound];
         uint4 va[kTokensPerRound], vb[kTokensPerRound];
         uint32_t rw[kTokensPerRound];
+    };
+    auto load_round = [&](int64_t t0, Round& r) {
 #pragma unroll
         for (int u = 0; u < kTokensPerRound; ++u) {
             const int64_t t = t0 + u * stride;
-            slot[u] = -1;
+            r.slot[u] = -1;
             if (t < num_tokens) {
-                slot[u] = __ldg(slot_mapping + t);
+                r.slot[u] = __ldg(slot_mapping + t);
                 const uint4* src = reinterpret_cast<const uint4*>(latent + t * latent_stride) + 2 * lane;
-                va[u] = __ldg(src);
-                vb[u] = __ldg(src + 1);
-                rw[u] = __ldg(reinterpret_cast<const uint32_t*>(rope + t * rope_stride) + lane);
+                r.va[u] = __ldg(src);
+                r.vb[u] = __ldg(src + 1);
+                r.rw[u] = __ldg(reinterpret_cast<const uint32_t*>(rope + t * rope_stride) + lane);
             }
         }
+    };
+    Round cur;
+    load_round(static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + warp, cur);
+    for (int64_t t0 = static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + warp; t0 < num_tokens;
+         t0 += stride * kTokensPerRound) {
+        Round nxt;
+        load_round(t0 + stride * kTokensPerRound, nxt);
+        const int64_t* slot = cur.slot;
+        const uint4* va = cur.va;
+        const uint4* vb = cur.vb;
+        const uint32_t* rw = cur.rw;
 #pragma unroll
         for (int u = 0; u < kTokensPerRound; ++u) {
             if (slot[u] < 0) continue;                       // padding token (or past the end)
@@ -218,6 +230,7 @@ quantize_append_kernel(const uint16_t* __restrict__ latent, int64_t latent_strid
             }
             __syncwarp();
         }
+        cur = nxt;
     }
 }
 
