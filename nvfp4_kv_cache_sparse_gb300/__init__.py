@@ -127,11 +127,12 @@ def quantize_append(kv_latent: torch.Tensor, k_rope: torch.Tensor, slot_mapping:
     _need(slot_mapping.dtype == torch.int64 and slot_mapping.is_contiguous(), "slot_mapping int64 contiguous")
     _need(cache.dtype == torch.uint8 and cache.dim() == 2 and cache.is_contiguous(), "cache uint8 [num_slots, R] contiguous")
     _need(cache.shape[1] in RECORD_BYTES, "record width must be 352, 432 or 656")
+    code = _record_code(cache, block_scales)
     for t in (kv_latent, k_rope, slot_mapping, cache):
         _need(t.is_cuda and t.device == cache.device, "all tensors on the same CUDA device")
     st = load().nvfp4_mla_quantize_append(
         _ptr(kv_latent), kv_latent.stride(0), _ptr(k_rope), k_rope.stride(0), _ptr(slot_mapping), T,
-        _ptr(cache), cache.shape[0], _record_code(cache, block_scales), _ptr(dev_status), _stream(stream))
+        _ptr(cache), cache.shape[0], code, _ptr(dev_status), _stream(stream))
     _check("nvfp4_mla_quantize_append", st)
 
 
@@ -157,6 +158,7 @@ def sparse_mla_decode(q: torch.Tensor, cache: torch.Tensor, indices: torch.Tenso
     topk = indices.shape[2]
     _need(cache.dtype == torch.uint8 and cache.dim() == 2 and cache.is_contiguous() and cache.shape[1] in RECORD_BYTES,
           "cache uint8 [N, 352|432|656] contiguous")
+    code = _record_code(cache, block_scales)
     if attn_sink is not None:
         _need(attn_sink.dtype == torch.float32 and attn_sink.numel() == h_q and attn_sink.is_contiguous(), "attn_sink fp32 [h_q]")
     if out is None:
@@ -167,7 +169,6 @@ def sparse_mla_decode(q: torch.Tensor, cache: torch.Tensor, indices: torch.Tenso
     _need(lse.dtype == torch.float32 and lse.is_contiguous() and tuple(lse.shape) == (B, s_q, h_q), "lse fp32 [B,s_q,h_q]")
     for t in (q, cache, indices, out, lse) + ((attn_sink,) if attn_sink is not None else ()):
         _need(t.is_cuda and t.device == q.device, "all tensors on the same CUDA device")
-    code = _record_code(cache, block_scales)
     need = workspace_size(B, s_q, h_q, topk, code, num_splits)
     if need and (workspace is None or workspace.numel() * workspace.element_size() < need):
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
