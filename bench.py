@@ -498,6 +498,35 @@ class OracleStep:
         return self.rows
 
 
+def oracle_decode_rate(w: synth.DecodeWorkload, n_rows: int = 4, block_scales: bool = False) -> dict:
+    """The oracle's decode rate on a sample of a configuration's query rows (CPU, fp64), for the
+    sweep lines: records of the sampled rows' slots are built first and not timed."""
+    import oracle
+    rows = synth.sample_rows(w, min(n_rows, w.n_rows))
+    slots, q, idx = synth.compact_for_rows(w, rows)
+    lat, rope = synth.pool_rows(w.pool_seed, torch.from_numpy(slots))
+    recs = oracle.quantize_records(synth.bf16_bits(lat), synth.bf16_bits(rope), w.record_bytes,
+                                   block_scales=block_scales)
+    sink = None if w.attn_sink is None else w.attn_sink.numpy()
+    t0 = time.perf_counter()
+    oracle.sparse_mla_decode(synth.bf16_bits(q), recs, idx, w.sm_scale, attn_sink=sink, block_scales=block_scales)
+    el = time.perf_counter() - t0
+    return {"oracle_query_tokens_per_s": rows.size / el, "oracle_cores": oracle.threads_available(),
+            "oracle_sample": f"{rows.size} of {w.n_rows} query rows (all heads, all keys)"}
+
+
+def oracle_append_rate(ww, n_tokens: int = 2048) -> dict:
+    """The oracle's append rate on the first n_tokens of a write workload (CPU)."""
+    import oracle
+    n = min(n_tokens, ww.T)
+    cache = np.zeros((n, ww.record_bytes), dtype=np.uint8)
+    lat, rope = synth.bf16_bits(ww.latent[:n]), synth.bf16_bits(ww.rope[:n])
+    t0 = time.perf_counter()
+    oracle.quantize_append(lat, rope, np.arange(n, dtype=np.int64), cache)
+    el = time.perf_counter() - t0
+    return {"oracle_tokens_per_s": n / el, "oracle_sample": f"{n} of {ww.T} tokens"}
+
+
 def cpu_baseline(args, w):
     import oracle
     rows = np.arange(w.n_rows)
@@ -633,7 +662,8 @@ def run_sweep(args):
                           "query_tokens_per_s_cold": w.n_rows / cold, "roofline_us": t_roof * 1e6,
                           "roofline_frac_cold": t_roof / cold, "bound": "tensor" if flops / (tflops * 1e12) >
                           bytes_ / (hbm * 1e9) else "hbm", "algorithmic_flops": flops, "algorithmic_bytes": bytes_,
-                          "valid_index_fraction": valid / w.indices.numel(), "peaks": peak_src}), flush=True)
+                          "valid_index_fraction": valid / w.indices.numel(), "peaks": peak_src,
+                          **oracle_decode_rate(w)}), flush=True)
         del cache
         torch.cuda.empty_cache()
     # scale-layout comparison (FlashMLA PR 18, format block: the permuted scale placement is
@@ -705,7 +735,7 @@ def run_write(ww, dev, iters, flush, hbm, peak_src):
                       "us_per_call_warm": warm * 1e6, "us_per_call_cold": cold * 1e6,
                       "tokens_per_s_cold": ww.T / cold, "achieved_gbs_cold": bytes_ / cold / 1e9,
                       "roofline_us": t_roof * 1e6, "roofline_frac_cold": t_roof / cold, "bound": "hbm",
-                      "algorithmic_bytes": bytes_, "peaks": peak_src}), flush=True)
+                      "algorithmic_bytes": bytes_, "peaks": peak_src, **oracle_append_rate(ww)}), flush=True)
     del cache
     torch.cuda.empty_cache()
 

@@ -30,3 +30,14 @@ def test_reference_arm_prints_one_contract_line():
     e2e = d["e2e"]
     assert e2e["value"] == d["value"] and e2e["unit"] == d["unit"]
     assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
+
+
+def test_sweep_oracle_rates_on_cpu():
+    sys.path.insert(0, ROOT)
+    import bench
+    import synth
+    r = bench.oracle_decode_rate(synth.tiny_decode(seed=0))
+    assert r["oracle_query_tokens_per_s"] > 0 and r["oracle_cores"] >= 1
+    assert r["oracle_sample"].startswith("1 of 1 query rows")
+    a = bench.oracle_append_rate(synth.write_path(seed=0, T=256, num_slots=1024), n_tokens=128)
+    assert a["oracle_tokens_per_s"] > 0 and a["oracle_sample"] == "128 of 256 tokens"
