@@ -29,6 +29,24 @@ def test_header_declares_the_expected_calls():
     assert set(syms) == set(lib.EXPORTED), syms
 
 
+def test_header_compiles_as_strict_c99(tmp_path):
+    # the boundary is a C ABI: the header must stand alone in a C translation unit
+    src = tmp_path / "use_header.c"
+    src.write_text('#include "nvfp4_mla.h"\n'
+                   "int main(void) {\n"
+                   "    size_t n = 0;\n"
+                   "    return nvfp4_sparse_mla_decode_workspace_size(1, 1, 64, 64, 352, 1, &n);\n"
+                   "}\n")
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    r = subprocess.run([cc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic", "-fsyntax-only",
+                        "-I", os.path.dirname(HEADER), str(src)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+
+
 def test_binding_constants_match_the_header():
     text = open(HEADER).read()
     m = re.search(r"#define NVFP4_MLA_SCALES_BLOCK_ORDER (0x[0-9a-fA-F]+)", text)
