@@ -47,6 +47,40 @@ def test_header_compiles_as_strict_c99(tmp_path):
     assert r.returncode == 0, r.stderr
 
 
+def test_a_c_program_links_and_calls_the_host_side_entry_points(tmp_path, cdll):
+    # a C caller, linked against the shared library, gets the documented host-side answers
+    # (no call here needs a GPU)
+    src = tmp_path / "caller.c"
+    src.write_text(r"""
+#include <stdio.h>
+#include <string.h>
+#include "nvfp4_mla.h"
+int main(void) {
+    size_t n = 1;
+    if (nvfp4_sparse_mla_decode_workspace_size(2, 1, 64, 64, 352, 1, &n) != NVFP4_MLA_OK || n != 0) return 1;
+    if (nvfp4_sparse_mla_decode_workspace_size(2, 1, 64, 64, 656, 2, &n) != NVFP4_MLA_OK ||
+        n != (size_t)2 * 2 * 64 * 512 * 2 + 1024) return 2;
+    if (nvfp4_sparse_mla_decode_workspace_size(1, 1, 64, 64, 400, 1, &n) != NVFP4_MLA_ERR_UNSUPPORTED) return 3;
+    if (nvfp4_mla_quantize_append(NULL, 512, NULL, 64, NULL, 0, NULL, 0, 352, NULL, NULL) != NVFP4_MLA_OK) return 4;
+    if (nvfp4_mla_status_string(NVFP4_MLA_OK) == NULL || nvfp4_mla_version() <= 0) return 5;
+    printf("ok %s\n", nvfp4_mla_status_string(NVFP4_MLA_ERR_WORKSPACE));
+    return 0;
+}
+""")
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    libdir = os.path.dirname(lib.library_path())
+    exe = tmp_path / "caller"
+    r = subprocess.run([cc, "-std=c99", "-Wall", "-Werror", "-I", os.path.dirname(HEADER), str(src), "-o", str(exe),
+                        "-L", libdir, "-lnvfp4mla", "-Wl,-rpath," + libdir], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    run = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert run.returncode == 0 and run.stdout.startswith("ok "), (run.returncode, run.stdout, run.stderr)
+
+
 def test_binding_constants_match_the_header():
     text = open(HEADER).read()
     m = re.search(r"#define NVFP4_MLA_SCALES_BLOCK_ORDER (0x[0-9a-fA-F]+)", text)
