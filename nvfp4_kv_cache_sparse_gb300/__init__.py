@@ -19,6 +19,8 @@ RECORD_BYTES = (352, 432, 656)
 # OR-ed into record_bytes: a 352-byte record whose scales are stored in block order (the
 # unpermuted side of the scale-layout comparison); the cache is still [N, 352]
 SCALES_BLOCK_ORDER = 0x10000
+# size of the library-owned scratch of nvfp4_sparse_mla_decode_no_alloc
+NO_ALLOC_SCRATCH_BYTES = 32 << 20
 D_NOPE, D_ROPE, D_QK, D_V = 512, 64, 576, 512
 
 OK = 0

@@ -85,6 +85,12 @@ def test_binding_constants_match_the_header():
     text = open(HEADER).read()
     m = re.search(r"#define NVFP4_MLA_SCALES_BLOCK_ORDER (0x[0-9a-fA-F]+)", text)
     assert m and int(m.group(1), 16) == lib.SCALES_BLOCK_ORDER
+    m = re.search(r"#define NVFP4_MLA_NO_ALLOC_SCRATCH_BYTES \(\(\(size_t\)(\d+)\) << (\d+)\)", text)
+    assert m and int(m.group(1)) << int(m.group(2)) == lib.NO_ALLOC_SCRATCH_BYTES
+    for name, value in (("SLOT_OUT_OF_RANGE", lib.DEV_SLOT_OUT_OF_RANGE), ("INDEX_OUT_OF_RANGE", lib.DEV_INDEX_OUT_OF_RANGE),
+                        ("TIMEOUT", lib.DEV_TIMEOUT), ("FP8_RANGE", lib.DEV_FP8_RANGE)):
+        m = re.search(r"#define NVFP4_MLA_DEV_%s (0x[0-9a-fA-F]+)u" % name, text)
+        assert m and int(m.group(1), 16) == value, name
 
 
 def test_library_exports_every_declared_symbol(cdll):
@@ -128,6 +134,14 @@ def test_host_side_checks_return_codes_without_a_device(cdll):
         assert cdll.nvfp4_sparse_mla_decode_workspace_size(2, 1, 64, 64, bad, 2, ctypes.byref(n)) == lib.ERR_UNSUPPORTED
         assert cdll.nvfp4_mla_quantize_append(None, 512, None, 64, None, 4, None, 8, bad, None, None) == lib.ERR_UNSUPPORTED
     assert cdll.nvfp4_mla_quantize_append(None, 512, None, 64, None, 4, None, 8, 352 | blk, None, None) == lib.ERR_INVALID_ARG
+    # the no-allocation decode refuses a problem whose partials exceed its fixed scratch, and
+    # passes the shape checks through, before any CUDA call
+    big = 64 * 64 * 128 * 512 * 2                 # 64 rows x 64 splits x 128 heads of f16 partials
+    assert big > lib.NO_ALLOC_SCRATCH_BYTES
+    assert cdll.nvfp4_sparse_mla_decode_no_alloc(None, None, 8, 352, None, 64, 1, 128, 4096, 1.0, None, None, None,
+                                                 64, None, None) == lib.ERR_WORKSPACE
+    assert cdll.nvfp4_sparse_mla_decode_no_alloc(None, None, 8, 400, None, 1, 1, 128, 64, 1.0, None, None, None,
+                                                 1, None, None) == lib.ERR_UNSUPPORTED
     # decode: null pointers
     assert cdll.nvfp4_sparse_mla_decode(None, None, 8, 352, None, 1, 1, 64, 64, 1.0, None, None, None, 1, None, 0,
                                         None, None) == lib.ERR_INVALID_ARG
