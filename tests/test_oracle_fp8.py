@@ -165,3 +165,19 @@ def test_decode_brute_force_against_scipy_softmax(with_sink):
             w = scipy.special.softmax(np.append(z, float(sink[h])))[:-1] if with_sink else scipy.special.softmax(z)
             assert lse[t, h] == pytest.approx(scipy.special.logsumexp(z), rel=1e-12, abs=1e-12)
             assert np.allclose(out[t, h], w @ keys[used, :512], rtol=1e-10, atol=1e-10 * np.abs(keys).max())
+
+
+def test_e4m3_encode_of_arbitrary_fp32_quotients_matches_torch():
+    # the fp8 record encodes fp32 quotients with up to 24 significant bits (not only bf16 values):
+    # random magnitudes over the whole e4m3 range, exact ties between neighbouring codes, and
+    # values one fp32 ulp either side of those ties
+    rng = np.random.default_rng(17)
+    mag = np.ldexp(rng.uniform(1.0, 2.0, 200_000), rng.integers(-12, 9, 200_000)).astype(np.float32)
+    mag = mag[mag <= 448.0]
+    codes = np.arange(0x00, 0x7E, dtype=np.uint8)
+    lo, hi = e4m3_value(codes), e4m3_value(codes + 1)
+    ties = ((lo + hi) / 2).astype(np.float32)
+    near = np.concatenate([ties, np.nextafter(ties, np.float32(0)), np.nextafter(ties, np.float32(1e9))])
+    x = np.concatenate([mag, near])
+    x = np.concatenate([x, -x]).astype(np.float32)
+    assert np.array_equal(oracle.e4m3_encode(x), torch_e4m3(x))
