@@ -440,3 +440,99 @@ __device__ __forceinline__ void cp_async_wait() {
 }
 
 }  // namespace nvfp4mla
+
+namespace nvfp4mla {
+
+// ---------------------------------------------------------------------------------------
+// tcgen05 with cta_group::2 (a CTA pair shares each MMA: every CTA supplies half of the A rows
+// and half of the B columns from its own shared memory, and receives its A rows' results in its
+// own tensor memory). Every tcgen05 instruction of a kernel uses the same cta_group.
+// ---------------------------------------------------------------------------------------
+
+// Warp-collective, executed by one warp in each CTA of the pair.
+__device__ __forceinline__ void tmem_alloc_cg2(uint32_t* dst, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(dst)),
+                 "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_cg2() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_cg2(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// D[tmem] (+)= A[smem] * B[smem], issued by one thread of the even CTA for the pair.
+__device__ __forceinline__ void mma_ss_cg2(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                           uint32_t accumulate) {
+    asm volatile(
+        "{\n"
+        "  .reg .pred p;\n"
+        "  setp.ne.b32 p, %4, 0;\n"
+        "  tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n"
+        "}\n" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate));
+}
+
+// D[tmem] (+)= A[tmem] * B[smem]. With M = 128 over the pair, the A rows of a CTA must be present
+// in both halves of its tensor memory lanes (lanes 0-63 feed the first N/2 columns of D, lanes
+// 64-127 the second N/2).
+__device__ __forceinline__ void mma_ts_cg2(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                           uint32_t accumulate) {
+    asm volatile(
+        "{\n"
+        "  .reg .pred p;\n"
+        "  setp.ne.b32 p, %4, 0;\n"
+        "  tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n"
+        "}\n" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate));
+}
+
+// Arrives once on the mbarrier at the same offset in each CTA named by `cta_mask` when every MMA
+// issued so far by this thread has completed.
+__device__ __forceinline__ void mma_commit_cg2(uint64_t* bar, uint16_t cta_mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            smem_addr(bar)),
+        "h"(cta_mask)
+        : "memory");
+}
+
+// 32 lanes x 16 consecutive 32-bit columns.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+
+// Named barrier over `threads` threads that also returns whether `pred` was true in any of them.
+__device__ __forceinline__ bool bar_red_or(uint32_t id, uint32_t threads, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n"
+        "  .reg .pred p, q;\n"
+        "  setp.ne.u32 p, %1, 0;\n"
+        "  barrier.red.or.pred q, %2, %3, p;\n"
+        "  selp.u32 %0, 1, 0, q;\n"
+        "}\n"
+        : "=r"(r)
+        : "r"(pred ? 1u : 0u), "r"(id), "r"(threads)
+        : "memory");
+    return r != 0;
+}
+
+// Asynchronous 4-byte store into a peer CTA's shared memory (complete_tx on the peer's mbarrier).
+__device__ __forceinline__ void st_async_b32(uint32_t cluster_saddr, uint32_t v, uint32_t cluster_mbar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(cluster_saddr),
+                 "r"(v), "r"(cluster_mbar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
+}  // namespace nvfp4mla

@@ -1162,32 +1162,35 @@ cudaError_t launch_wait_timeout_probe(uint32_t* status, uint64_t* elapsed_ns, cu
 }
 
 cudaError_t launch_sparse_decode(const DecodeArgs& d, cudaStream_t stream) {
-    KernelArgs a;
-    if (!encode_cache_map(&a.tmap, d.cache, d.num_slots, d.record_bytes)) return cudaErrorInvalidValue;
-    if (!encode_q_map(&a.qmap, d.q, static_cast<int64_t>(d.rows) * d.h_q)) return cudaErrorInvalidValue;
-    a.q = static_cast<const uint16_t*>(d.q);
-    a.cache = d.cache;
-    a.num_slots = d.num_slots;
-    a.indices = d.indices;
-    a.h_q = d.h_q;
-    a.topk = d.topk;
-    a.splits = d.splits;
-    a.keys_per_split = decode_keys_per_split(d.topk, d.splits);
-    a.scale_log2 = d.sm_scale * kLog2e;
-    a.sink = d.attn_sink;
-    a.out = static_cast<__nv_bfloat16*>(d.out);
-    a.lse = d.lse;
-    a.part_out = d.part_out;
-    a.part_lse = d.part_lse;
-    a.status = d.dev_status;
-    const dim3 grid(static_cast<unsigned>(d.rows) * static_cast<unsigned>(d.splits) * 2u);
-    const dim3 block(kThreads);
-    cudaError_t err = d.record_bytes == 656 ? prepare_kernel<656, false>()
-                      : d.record_bytes == 432 ? prepare_kernel<432, false>()
-                      : d.block_scales      ? prepare_kernel<352, true>()
-                                            : prepare_kernel<352, false>();
-    if (err != cudaSuccess) return err;
-    {
+    cudaError_t err;
+    if (decode_pair_supported(d)) {
+        err = launch_decode_pair(d, stream);
+    } else {
+        KernelArgs a;
+        if (!encode_cache_map(&a.tmap, d.cache, d.num_slots, d.record_bytes)) return cudaErrorInvalidValue;
+        if (!encode_q_map(&a.qmap, d.q, static_cast<int64_t>(d.rows) * d.h_q)) return cudaErrorInvalidValue;
+        a.q = static_cast<const uint16_t*>(d.q);
+        a.cache = d.cache;
+        a.num_slots = d.num_slots;
+        a.indices = d.indices;
+        a.h_q = d.h_q;
+        a.topk = d.topk;
+        a.splits = d.splits;
+        a.keys_per_split = decode_keys_per_split(d.topk, d.splits);
+        a.scale_log2 = d.sm_scale * kLog2e;
+        a.sink = d.attn_sink;
+        a.out = static_cast<__nv_bfloat16*>(d.out);
+        a.lse = d.lse;
+        a.part_out = d.part_out;
+        a.part_lse = d.part_lse;
+        a.status = d.dev_status;
+        const dim3 grid(static_cast<unsigned>(d.rows) * static_cast<unsigned>(d.splits) * 2u);
+        const dim3 block(kThreads);
+        err = d.record_bytes == 656 ? prepare_kernel<656, false>()
+              : d.record_bytes == 432 ? prepare_kernel<432, false>()
+              : d.block_scales      ? prepare_kernel<352, true>()
+                                    : prepare_kernel<352, false>();
+        if (err != cudaSuccess) return err;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = grid;
         cfg.blockDim = block;
@@ -1205,10 +1208,14 @@ cudaError_t launch_sparse_decode(const DecodeArgs& d, cudaStream_t stream) {
                             : d.block_scales      ? sparse_decode_kernel<352, true>
                                                   : sparse_decode_kernel<352, false>;
         err = cudaLaunchKernelEx(&cfg, kernel, a);
+        if (err == cudaSuccess) err = cudaGetLastError();
     }
-    if (err == cudaSuccess) err = cudaGetLastError();
     if (err != cudaSuccess || d.splits == 1) return err;
-    // the merge launches while the decode grid runs and waits for it on the device
+    return launch_split_merge(d, stream);
+}
+
+// The merge launches while the decode grid runs and waits for it on the device.
+cudaError_t launch_split_merge(const DecodeArgs& d, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
     const int rows_heads = d.rows * d.h_q;
     cfg.gridDim = dim3(static_cast<unsigned>((rows_heads + 7) / 8));
