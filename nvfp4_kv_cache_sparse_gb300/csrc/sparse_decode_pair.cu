@@ -17,9 +17,10 @@
 //   P V: M = 128 (heads) x N = 256 x K = 128 (keys) pair MMAs; CTA 0 supplies V dims 0-255 and
 //     CTA 1 dims 256-511, each for all 128 keys, so O of a CTA's 64 heads spans all 512 dims
 //     (lanes 0-63: dims 0-255, lanes 64-127: dims 256-511) in 256 tensor-memory columns.
-//   Every record is loaded once per pair. A CTA dequantizes its own keys' K rows (576 dims) and
-//   the V rows of its own half of the dims for all 128 keys; the raw e2m1 codes and scales of the
-//   other CTA's half of the dims cross to it over DSMEM (36 bytes per key and thread quarter).
+//   A CTA dequantizes its own keys' K rows (576 dims) from their whole records, and the V rows of
+//   its own half of the dims for all 128 keys from that half's codes and scales. Both CTAs read
+//   the V half of a record around the time its owner reads the whole, so DRAM delivers each
+//   record once per pair and the second read comes from L2.
 // Numbers. e2m1 x e4m3 products are exact in f16 (<= 5 significant bits in [2^-10, 2688]), so K
 // and V tiles are f16 (the bf16 RoPE of 432-byte records stays bf16). q enters as f16 scaled by a
 // per-head power of two (2^pre with max|q| 2^pre in [2^14, 2^15)): the products q_d K_d are the
@@ -33,9 +34,12 @@
 // Warp roles (kThreads = 832, 26 warps):
 //   0-7   softmax (warp w: lane quadrant w & 3, score columns 32 (w >> 2)..+32); q staging in the
 //         prologue; output in the epilogue
-//   8-15  K converters: load own records (registers, one tile ahead, L2 prefetch two ahead), write
-//         K rows, the own-half raw codes (local) and the other half's raw codes (to the peer)
-//   16-23 V converters: V rows of this CTA's dims for all 128 keys, from the two raw buffers
+//   8-15  K converters: K rows of the own keys, blocks 0-3 as soon as the previous QK has read
+//         its first half, blocks 4-8 once it has finished
+//   16-23 V converters: V rows of keys 0-63 once the previous PV has read them, then of keys
+//         64-127; they also help to stage q
+//         Converter threads stage the record bytes they convert with cp.async one tile ahead, so
+//         no load sits between a thread's conversion and its arrive
 //   24    QK issuer (CTA 0) and tensor-memory owner (both)
 //   25    PV issuer (CTA 0)
 // Every wait is bounded by time; on timeout a CTA sets NVFP4_MLA_DEV_TIMEOUT, stops issuing work,
@@ -75,40 +79,52 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units
 // Shared memory (offsets from a 1024-byte aligned base)
 constexpr int kBlk = 8192;                 // 64 rows x 128 B (one 64-wide 16-bit block)
 constexpr int kVBlk = 16384;               // 128 rows x 128 B
-constexpr int kOffXmax = 1024;             // float [4][64] tile maxima (slow path) / row sums
-constexpr int kOffXl = 2048;               // float [4][64]
+constexpr int kOffXmax = 512;              // float [8][64]: maxima of q, tile maxima (slow path)
+constexpr int kOffXl = 2560;               // float [4][64]: row sums
 constexpr int kOffK = 4096;                // 9 blocks: K rows of the 64 own keys (K-major)
 constexpr int kOffV = kOffK + 9 * kBlk;    // 4 blocks of 128 keys: this CTA's 256 V dims (MN-major)
 constexpr int kOffP = kOffV + 4 * kVBlk;   // 2 blocks: P [64 heads x 128 keys] (K-major)
 constexpr int kOffQs = kOffP + 2 * kBlk;   // 3 blocks: q dims [384, 576)
-constexpr int kRawCodes = kOwn * 4 * 32;   // [key][quarter] 32 B of e2m1 codes
-constexpr int kRawBytes = kRawCodes + kOwn * 4 * 4;   // + [key][quarter] 4 scale bytes
-constexpr int kOffOwnRaw = kOffQs + 3 * kBlk;         // [2] own keys, this CTA's dims
-constexpr int kOffPeerRaw = kOffOwnRaw + 2 * kRawBytes;   // [2] the peer's keys, this CTA's dims
-constexpr int kSmemBytes = kOffPeerRaw + 2 * kRawBytes;
-constexpr int kSmemAlloc = kSmemBytes + 1024;
-static_assert(kSmemAlloc <= 232448, "shared memory");
+// Staging (cp.async, one tile ahead; entry strides are 8 words modulo 32 banks, so the 64-bit reads
+// of a quarter-warp's 4 keys x 4 quarters meet 32 different banks, except 144-byte V entries):
+//   a: [64 own keys] record bytes 0-127 (codes of blocks 0-15), then the 32 scale bytes
+//   b: [64 own keys] record bytes 128-255 (codes of blocks 16-31), then the RoPE bytes
+//   v: [2 halves][64 keys] this CTA's 128 code bytes (record bytes 128 crank ..), then the 16 scale
+//      bytes of its 32 blocks
+constexpr int kStrA = 160;
+template <int R> constexpr int kStrB = R == 352 ? 224 : 288;
+template <int R> constexpr int kStrV = R == 352 ? 160 : 144;
+constexpr int kOffStA = kOffQs + 3 * kBlk;
+constexpr int kOffStB = kOffStA + kOwn * kStrA;
+template <int R> constexpr int kOffStV = kOffStB + kOwn * kStrB<R>;
+template <int R> constexpr int kSmemBytes = kOffStV<R> + 2 * kOwn * kStrV<R>;
+template <int R> constexpr int kSmemAlloc = kSmemBytes<R> + 1024;
+static_assert(kSmemAlloc<352> <= 232448 && kSmemAlloc<432> <= 232448, "shared memory");
 static_assert(kOffK % 1024 == 0 && kOffV % 1024 == 0 && kOffP % 1024 == 0 && kOffQs % 1024 == 0, "operand alignment");
 static_assert(9 * kBlk <= 4 * kVBlk + 2 * kBlk, "q staging fits in the V and P buffers");
 static_assert(kHeads * 1024 <= 9 * kBlk, "output staging fits in the K buffer");
 
+// Buffers are handed back in halves so that converters refill one half while the MMAs still
+// read the other: K blocks 0-3 (dims 0-255) and 4-8, V rows / P columns of keys 0-63 and 64-127.
 struct __align__(8) Ctl {
+    uint64_t khalf;           // QK commit after dims 0-255 (multicast): K blocks 0-3 free
     uint64_t qkdone;          // QK commit (multicast): S ready, K buffer free
+    uint64_t pvhalf;          // PV commit after keys 0-63 (multicast): V rows / P columns 0-63 free
     uint64_t pvdone;          // PV commit (multicast): V and P buffers free, O updated
-    uint64_t kfull;           // CTA 0: 16 warps (8 per CTA) wrote K rows
-    uint64_t vfull;           // CTA 0: 16 warps wrote V rows
+    uint64_t kfull_a;         // CTA 0: 16 warps (8 per CTA) wrote K blocks 0-3
+    uint64_t kfull_b;         // CTA 0: 16 warps wrote K blocks 4-8
+    uint64_t vfull_a;         // CTA 0: 16 warps wrote V rows 0-63
+    uint64_t vfull_b;         // CTA 0: 16 warps wrote V rows 64-127
     uint64_t sfree;           // CTA 0: 16 softmax warps read S
-    uint64_t pfull;           // CTA 0: 16 softmax warps wrote P (and rescaled O)
-    uint64_t qready;          // CTA 0: 16 softmax warps put q into tensor and shared memory
-    uint64_t qstaged;         // 8 local softmax warps finished reading the q staging area
+    uint64_t pfull_a;         // CTA 0: 16 softmax warps: P columns 0-63 written, O rescaled
+    uint64_t pfull_b;         // CTA 0: 8 softmax warps (lanes 64-127) wrote P columns 64-127
+    uint64_t qready;          // CTA 0: 32 warps (16 per CTA) put q into tensor and shared memory
+    uint64_t qstaged;         // 16 local warps finished reading the q staging area
     uint64_t qload;           // q boxes landed (TMA, tx-counted)
-    uint64_t own_full[2];     // K converters wrote own raw codes
-    uint64_t own_empty[2];    // V converters read them
-    uint64_t peer_full[2];    // the peer's raw codes landed (st.async, tx-counted)
-    uint64_t peer_empty[2];   // the peer's V converters read what this CTA sent (remote arrivals)
     uint64_t drain;           // CTA 0: both issuers' MMAs completed
     uint32_t tmem_base;
     uint32_t abort;
+    uint32_t sig_sink;        // target of the 4-byte st.async signals (the value is never read)
 };
 static_assert(sizeof(Ctl) <= kOffXmax, "control block");
 
@@ -142,9 +158,18 @@ __device__ __forceinline__ void set_abort(Ctl* ctl, uint32_t* status) {
 }
 __device__ __forceinline__ bool aborted(Ctl* ctl) { return *reinterpret_cast<volatile uint32_t*>(&ctl->abort) != 0u; }
 
-// Bounded wait, cluster-scope acquire (several barriers here receive arrivals or bytes from the
-// peer CTA). One answer per warp.
+// Bounded wait, one answer per warp. CTA-scope acquire for barriers that this CTA's threads or the
+// pair's MMA commits complete; cluster-scope acquire (wait_peer) for those that the peer CTA's
+// st.async data or signals complete.
 __device__ __forceinline__ bool wait_warp(Ctl* ctl, uint64_t* bar, uint32_t parity, uint32_t* status) {
+    bool ok = mbar_try_wait(bar, parity);
+    if (!ok && !aborted(ctl)) {
+        ok = mbar_wait(bar, parity);
+        if (!ok) set_abort(ctl, status);
+    }
+    return __all_sync(0xffffffffu, ok);
+}
+__device__ __forceinline__ bool wait_peer(Ctl* ctl, uint64_t* bar, uint32_t parity, uint32_t* status) {
     bool ok = mbar_try_wait_cluster(bar, parity);
     if (!ok && !aborted(ctl)) {
         ok = mbar_wait_cluster(bar, parity);
@@ -153,12 +178,20 @@ __device__ __forceinline__ bool wait_warp(Ctl* ctl, uint64_t* bar, uint32_t pari
     return __all_sync(0xffffffffu, ok);
 }
 
-// Arrival on a barrier that lives in CTA 0 (the pair's MMA issuer), from either CTA.
-__device__ __forceinline__ void arrive_leader(uint64_t* bar, int crank) {
-    if (crank == 0)
-        mbar_arrive(bar);
-    else
-        mbar_arrive_cluster(mapa_shared(smem_addr(bar), 0));
+// A warp's signal (lane 0) on a barrier that lives in CTA 0, the pair's MMA issuer. CTA 0's warps
+// arrive (one of them, `arm` true, also registers the 4 bytes that each of CTA 1's `n_peer` warps
+// sends); CTA 1's warps send 4 bytes with complete_tx. The send is asynchronous: the warp does not
+// wait until its earlier writes are visible across the cluster, as a remote release arrive would
+// (the complete_tx carries release semantics at cluster scope).
+__device__ __forceinline__ void signal_leader(Ctl* ctl, uint64_t* bar, int crank, bool arm, uint32_t n_peer) {
+    if (crank == 0) {
+        if (arm)
+            mbar_arrive_expect_tx(bar, 4u * n_peer);
+        else
+            mbar_arrive(bar);
+    } else {
+        st_async_b32(mapa_shared(smem_addr(&ctl->sig_sink), 0), 0u, mapa_shared(smem_addr(bar), 0));
+    }
 }
 
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
@@ -181,17 +214,19 @@ __device__ __forceinline__ __half2 scale_half2(uint32_t sbyte) {
 // Eight e2m1 codes (one word, low nibble first) times a scale -> four f16x2 words (exact).
 __device__ __forceinline__ uint4 dq8(uint32_t w, __half2 s2) {
     uint32_t h[4];
+    asm("{\n"
+        "  .reg .b8 a, b, c, d;\n"
+        "  mov.b32 {a, b, c, d}, %4;\n"
+        "  cvt.rn.f16x2.e2m1x2 %0, a;\n"
+        "  cvt.rn.f16x2.e2m1x2 %1, b;\n"
+        "  cvt.rn.f16x2.e2m1x2 %2, c;\n"
+        "  cvt.rn.f16x2.e2m1x2 %3, d;\n"
+        "}\n"
+        : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+        : "r"(w));
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-        uint32_t v;
-        asm("{\n"
-            "  .reg .b8 t;\n"
-            "  cvt.u8.u32 t, %1;\n"
-            "  cvt.rn.f16x2.e2m1x2 %0, t;\n"
-            "}\n"
-            : "=r"(v)
-            : "r"(w >> (8 * k)));
-        const __half2 p = __hmul2(*reinterpret_cast<__half2*>(&v), s2);
+        const __half2 p = __hmul2(*reinterpret_cast<const __half2*>(&h[k]), s2);
         h[k] = *reinterpret_cast<const uint32_t*>(&p);
     }
     return make_uint4(h[0], h[1], h[2], h[3]);
@@ -205,60 +240,13 @@ __device__ __forceinline__ uint2 e4m3x4_to_f16(uint32_t w) {
     return make_uint2(a, b);
 }
 
-// The bytes of one own key that one converter thread (quarter q) needs: e2m1 codes of the 16-wide
-// blocks 4c + q (c = 0..7; block s holds dims 16s..16s+15 at bytes 8s..8s+7), their eight scale
-// bytes (byte c = block 4c + q) and 16 RoPE dims 16q..16q+15 (e4m3 in one word-quad for 352-byte
-// records, bf16 in two for 432-byte records).
-struct Raw {
-    uint2 codes[8];
-    uint2 sc;
-    uint4 rope[2];
-};
-
-// kBlkOrder: the 32 scale bytes are in block order (432-byte records, and the 352-byte record of
-// the scale-layout comparison) instead of the permuted placement 8 (s & 3) + (s >> 2).
-template <int R, bool kBlkOrder>
-__device__ __forceinline__ void load_raw(const uint8_t* rec, int q, Raw& r) {
-#pragma unroll
-    for (int c = 0; c < 8; ++c) r.codes[c] = __ldg(reinterpret_cast<const uint2*>(rec + 32 * c + 8 * q));
-    if constexpr (R == 352 && !kBlkOrder) {
-        // permuted placement: blocks {4c + q, c = 0..7} are the eight bytes at 320 + 8q
-        r.sc = __ldg(reinterpret_cast<const uint2*>(rec + 320 + 8 * q));
-    } else {
-        const int sb = R == 352 ? 320 : 256;   // block s at byte sb + s
-        const uint4 a = __ldg(reinterpret_cast<const uint4*>(rec + sb));
-        const uint4 b = __ldg(reinterpret_cast<const uint4*>(rec + sb + 16));
-        const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};   // w[c] holds blocks 4c..4c+3
-        uint32_t lo = 0u, hi = 0u;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            lo |= ((w[c] >> (8 * q)) & 0xFFu) << (8 * c);
-            hi |= ((w[c + 4] >> (8 * q)) & 0xFFu) << (8 * c);
-        }
-        r.sc = make_uint2(lo, hi);
-    }
-    if constexpr (R == 352) {
-        r.rope[0] = __ldg(reinterpret_cast<const uint4*>(rec + 256 + 16 * q));
-        r.rope[1] = make_uint4(0u, 0u, 0u, 0u);
-    } else {
-        r.rope[0] = __ldg(reinterpret_cast<const uint4*>(rec + 304 + 32 * q));
-        r.rope[1] = __ldg(reinterpret_cast<const uint4*>(rec + 304 + 32 * q + 16));
-    }
+// Byte q of each word of w, low word first.
+__device__ __forceinline__ uint32_t gather_byte4(const uint4& w, int q) {
+    const uint32_t sel = static_cast<uint32_t>(q) | (static_cast<uint32_t>(q + 4) << 4);
+    return __byte_perm(__byte_perm(w.x, w.y, sel), __byte_perm(w.z, w.w, sel), 0x5410);
 }
 
-__device__ __forceinline__ void zero_raw(Raw& r) {
-#pragma unroll
-    for (int c = 0; c < 8; ++c) r.codes[c] = make_uint2(0u, 0u);
-    r.sc = make_uint2(0u, 0u);
-    r.rope[0] = r.rope[1] = make_uint4(0u, 0u, 0u, 0u);
-}
-
-// One thread's share of a raw buffer entry (key j, quarter q): the codes of blocks 4c + q for the
-// receiving CTA's four c (32 B) and their scale bytes (4 B).
-__device__ __forceinline__ uint32_t raw_codes_at(uint32_t buf, int j, int q) { return buf + (j * 4 + q) * 32; }
-__device__ __forceinline__ uint32_t raw_scale_at(uint32_t buf, int j, int q) { return buf + kRawCodes + (j * 4 + q) * 4; }
-
-// V rows: the four blocks 4c + q (c = 4 half + cl) of one key into V block cl, chunks 2q, 2q + 1.
+// V row of one key: the four blocks 4c + q (c = 4 half + cl) into V block cl, chunks 2q, 2q + 1.
 __device__ __forceinline__ void write_v(uint32_t v_s, int row, int q, const uint4& c01, const uint4& c23,
                                         uint32_t sbytes) {
     const uint32_t cw[8] = {c01.x, c01.y, c01.z, c01.w, c23.x, c23.y, c23.z, c23.w};
@@ -270,6 +258,8 @@ __device__ __forceinline__ void write_v(uint32_t v_s, int row, int q, const uint
     }
 }
 
+// kBlkOrder: the 32 scale bytes are in block order (432-byte records, and the 352-byte record of
+// the scale-layout comparison) instead of the permuted placement 8 (s & 3) + (s >> 2).
 template <int R, bool kBlkOrder>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     decode_pair_kernel(const __grid_constant__ KernelArgs a) {
@@ -290,27 +280,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int32_t* idx_row = a.indices + static_cast<int64_t>(row) * a.topk;
 
     if (threadIdx.x == 0) {
+        mbar_init(&ctl->khalf, 1);
         mbar_init(&ctl->qkdone, 1);
+        mbar_init(&ctl->pvhalf, 1);
         mbar_init(&ctl->pvdone, 1);
-        mbar_init(&ctl->kfull, 16);
-        mbar_init(&ctl->vfull, 16);
-        mbar_init(&ctl->sfree, 16);
-        mbar_init(&ctl->pfull, 16);
+        // CTA 0's own warps arrive on these; CTA 1's warps send 4 bytes each (complete_tx), which
+        // one arriving warp of CTA 0 registers with expect_tx
+        mbar_init(&ctl->kfull_a, 8);
+        mbar_init(&ctl->kfull_b, 8);
+        mbar_init(&ctl->vfull_a, 8);
+        mbar_init(&ctl->vfull_b, 8);
+        mbar_init(&ctl->sfree, 8);
+        mbar_init(&ctl->pfull_a, 8);
+        mbar_init(&ctl->pfull_b, 4);
         mbar_init(&ctl->qready, 16);
-        mbar_init(&ctl->qstaged, 8);
+        mbar_init(&ctl->qstaged, 16);
         mbar_init(&ctl->qload, 1);
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(&ctl->own_full[b], 8);
-            mbar_init(&ctl->own_empty[b], 8);
-            mbar_init(&ctl->peer_full[b], 1);
-            mbar_init(&ctl->peer_empty[b], 8);
-        }
         mbar_init(&ctl->drain, 2);
         ctl->abort = 0u;
         fence_barrier_init();
-        // the first two tiles' bytes from the peer may arrive as soon as the cluster barrier opens
-        if (n_tiles > 0) mbar_arrive_expect_tx(&ctl->peer_full[0], kRawBytes);
-        if (n_tiles > 1) mbar_arrive_expect_tx(&ctl->peer_full[1], kRawBytes);
     }
     if (warp == kWarpQK) {
         tmem_alloc_cg2(&ctl->tmem_base, kTmemCols);
@@ -327,77 +315,75 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     cluster_arrive();
     cluster_wait();   // both CTAs' barriers exist before any remote access
 
-    if (warp < 8) {
-        // ======================= softmax warps =======================
-        const int qd = warp & 3;               // TMEM lane quadrant
-        const int h2 = warp >> 2;              // score column half
-        const int L = 32 * qd + lane;          // TMEM lane
-        const int hl = L & 63;                 // head within the CTA
-        const int qi = ((qd >> 1) << 1) | h2;  // this thread's slot among the head's four
+    // ---- q: the softmax warps (0-7) and the V converters (16-23), idle until the first V tile,
+    // stage q: largest magnitude per head, the power-of-two prescale, f16 (or bf16 RoPE) copies in
+    // tensor memory (dims 0-383, both lane halves) and shared memory (dims 384-575).
+    const bool qwarp = warp < 8 || (warp >= kWarpV && warp < kWarpQK);
+    float ch = 0.0f;   // sm_scale log2(e) 2^-pre of this thread's head (softmax warps)
+    if (qwarp) {
+        const int qd = warp & 3;                                      // TMEM lane quadrant
+        const int g = (warp >= kWarpV ? 2 : 0) + ((warp >> 2) & 1);   // 0..3: warp of the quadrant
+        const int L = 32 * qd + lane;
+        const int hl = L & 63;
+        const int slot = ((qd >> 1) << 2) | g;                        // 0..7 among the head's threads
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * qd) << 16);
         float* xmax = reinterpret_cast<float*>(smem + kOffXmax);
-        float* xl = reinterpret_cast<float*>(smem + kOffXl);
-        // ---- q: largest magnitude of the head, the power-of-two prescale, f16 (or bf16 RoPE) copies
         if (threadIdx.x == 0) {
             mbar_arrive_expect_tx(&ctl->qload, 9u * kBlk);
             for (int bx = 0; bx < 9; ++bx)
                 tma_load_2d(sbase + kOffV + bx * kBlk, &a.qmap, 64 * bx, row * 128 + 64 * crank, &ctl->qload);
         }
-        bool ok = wait_warp(ctl, &ctl->qload, 0, a.status);
+        const bool okq = wait_warp(ctl, &ctl->qload, 0, a.status);
         const uint32_t stage = sbase + kOffV;   // box b (dims 64b..): head hl chunk c at b*8192 + swz(hl, c)
         float qmax = 0.0f;
-        if (ok) {
-#pragma unroll 1
-            for (int k = 18 * qi; k < 18 * qi + 18; ++k) {   // 72 chunks of 8 dims per head, 18 per thread
+        if (okq) {
+#pragma unroll 3
+            for (int k = 9 * slot; k < 9 * slot + 9; ++k) {   // 72 chunks of 8 dims per head, 9 per thread
                 const uint4 x = lds_u128(stage + (k >> 3) * kBlk + swz(hl, k & 7));
                 const uint32_t w[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                    qmax = fmaxf(qmax, fabsf(__uint_as_float(w[m] << 16)));
-                    qmax = fmaxf(qmax, fabsf(__uint_as_float(w[m] & 0xFFFF0000u)));
-                }
+                for (int m = 0; m < 4; ++m)
+                    qmax = fmax3(qmax, fabsf(__uint_as_float(w[m] << 16)), fabsf(__uint_as_float(w[m] & 0xFFFF0000u)));
             }
         }
-        xmax[qi * 64 + hl] = qmax;
-        named_bar_sync(1, 256);
-        qmax = fmaxf(fmaxf(xmax[hl], xmax[64 + hl]), fmaxf(xmax[128 + hl], xmax[192 + hl]));
+        xmax[slot * 64 + hl] = qmax;
+        named_bar_sync(2, 512);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) qmax = fmaxf(qmax, xmax[k * 64 + hl]);
         int pre = 0;
         if (qmax > 0.0f) {
             int e;
             frexpf(qmax, &e);   // qmax < 2^e <= 2 qmax
             pre = min(100, max(-100, 15 - e));
         }
-        const int p1 = pre / 2, p2 = pre - p1;
-        const float f1 = __int_as_float((127 + p1) << 23), f2 = __int_as_float((127 + p2) << 23);
-        // c = sm_scale log2(e) 2^-pre: S' = 2^pre S, so z = c S' (log2 domain)
-        const float ch = a.sm_scale * kLog2e * __int_as_float((127 - p1) << 23) * __int_as_float((127 - p2) << 23);
+        const float fpre = __int_as_float((127 + pre) << 23);
+        ch = a.sm_scale * kLog2e * __int_as_float((127 - pre) << 23);   // S' = 2^pre S, z = ch S'
         auto cvt_pair = [&](uint32_t w, bool bf) -> uint32_t {
-            const float lo = __uint_as_float(w << 16) * f1 * f2, hi = __uint_as_float(w & 0xFFFF0000u) * f1 * f2;
+            const float lo = __uint_as_float(w << 16) * fpre, hi = __uint_as_float(w & 0xFFFF0000u) * fpre;
             return bf ? pack_bf16x2(lo, hi) : pack_f16x2(lo, hi);
         };
-        if (ok) {
-            // dims [0, 384): TMEM columns kColQ.. in this lane (both lane halves hold a copy);
-            // this thread takes dims [192 h2, 192 h2 + 192) = 24 chunks
-#pragma unroll 1
-            for (int g = 0; g < 3; ++g) {
-                uint32_t v[32];
+        if (okq) {
+            // dims [0, 384) = 48 chunks into TMEM columns kColQ + 4 chunk: 12 chunks per warp of the quadrant
+            uint32_t v[16];
 #pragma unroll
-                for (int cc = 0; cc < 8; ++cc) {
-                    const int k = 24 * h2 + 8 * g + cc;   // dim chunk
+            for (int half = 0; half < 3; ++half) {   // 3 x 4 chunks = 12 chunks = 48 columns
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    const int k = 12 * g + 4 * half + cc;
                     const uint4 x = lds_u128(stage + (k >> 3) * kBlk + swz(hl, k & 7));
                     v[4 * cc + 0] = cvt_pair(x.x, false);
                     v[4 * cc + 1] = cvt_pair(x.y, false);
                     v[4 * cc + 2] = cvt_pair(x.z, false);
                     v[4 * cc + 3] = cvt_pair(x.w, false);
                 }
-                tmem_st32(lane_base + kColQ + 96 * h2 + 32 * g, v);
+                tmem_st16(lane_base + kColQ + 48 * g + 16 * half, v);
             }
-            // dims [384, 576) into shared memory (one copy: lanes 0-63), K-major blocks of 64 dims
+            // dims [384, 576) = chunks 48..71 into shared memory (one copy, lanes 0-63): 6 chunks per warp
             if (qd < 2) {
-#pragma unroll 1
-                for (int cc = 0; cc < 12; ++cc) {
-                    const int k = 48 + 12 * h2 + cc;      // dim chunk 48..71
-                    const bool bf = R == 432 && k >= 64;  // bf16 RoPE of 432-byte records
+#pragma unroll 2
+                for (int cc = 0; cc < 6; ++cc) {
+                    const int k = 48 + 6 * g + cc;
+                    const bool bf = R == 432 && k >= 64;   // bf16 RoPE of 432-byte records
                     const uint4 x = lds_u128(stage + (k >> 3) * kBlk + swz(hl, k & 7));
                     const uint4 y = make_uint4(cvt_pair(x.x, bf), cvt_pair(x.y, bf), cvt_pair(x.z, bf), cvt_pair(x.w, bf));
                     sts_u128(sbase + kOffQs + ((k - 48) >> 3) * kBlk + swz(hl, k & 7), y);
@@ -410,13 +396,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) {
             mbar_arrive(&ctl->qstaged);
-            arrive_leader(&ctl->qready, crank);
+            signal_leader(ctl, &ctl->qready, crank, warp == 0, 16);
         }
-        // ---- tiles
+    }
+
+    if (warp < 8) {
+        // ======================= softmax warps =======================
+        const int qd = warp & 3;               // TMEM lane quadrant
+        const int h2 = warp >> 2;              // score column half
+        const int L = 32 * qd + lane;          // TMEM lane
+        const int hl = L & 63;                 // head within the CTA
+        const int qi = ((qd >> 1) << 1) | h2;  // this thread's slot among the head's four
+        const bool upper = qd >= 2;            // lanes 64-127: keys 64-127 of a tile, dims 256-511 of O
+        const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * qd) << 16);
+        float* xmax = reinterpret_cast<float*>(smem + kOffXmax);
+        float* xl = reinterpret_cast<float*>(smem + kOffXl);
+        bool ok = !aborted(ctl);
         float m_ref = -INFINITY;   // reference max (log2 units), the same in the head's four threads
         float l = 0.0f;            // this thread's sum of 2^(z - m_ref)
         const bool pos_scale = a.sm_scale > 0.0f;
-        const uint32_t p_row = sbase + kOffP + (qd >> 1) * kBlk;
+        const uint32_t p_row = sbase + kOffP + (upper ? kBlk : 0);
         // Every softmax warp takes part in every named barrier below, also after a wait ran out
         // (then it only passes the barriers), so no warp can be left waiting on a missing one.
         for (int i = 0; i < n_tiles; ++i) {
@@ -430,7 +429,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 tmem_wait_ld();
                 tc_fence_before_sync();
                 __syncwarp();
-                if (lane == 0) arrive_leader(&ctl->sfree, crank);
+                if (lane == 0) signal_leader(ctl, &ctl->sfree, crank, warp == 0, 8);
                 float m0 = -INFINITY, m1 = -INFINITY;
                 if (pos_scale) {
 #pragma unroll
@@ -478,6 +477,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         tmem_wait_st();
                     }
                 }
+                // the tile maxima are read before anyone writes the next ones
+                named_bar_sync(1, 256);
             }
             if (!ok) continue;
             // ---- P = 2^(z - m_ref) in f16; masked keys (NaN scores) give 0
@@ -505,8 +506,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int j = 0; j < 16; ++j) pw[j] = 0u;
             }
-            // ---- P into shared memory once PV of the previous tile released it
-            if (i > 0) ok = wait_warp(ctl, &ctl->pvdone, (i - 1) & 1, a.status);
+            // ---- P columns of this warp's keys once PV of the previous tile released them. Lanes
+            // 64-127 report their O rescale done on pfull_a first (the first PV half writes O too).
+            if (upper) {
+                // (after the first half of the previous PV, so that this arrival cannot reach CTA 0's
+                // barrier while it still counts the previous tile)
+                if (i > 0) ok = wait_warp(ctl, &ctl->pvhalf, (i - 1) & 1, a.status);
+                if (!ok) continue;
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) signal_leader(ctl, &ctl->pfull_a, crank, false, 8);
+            }
+            if (i > 0) ok = wait_warp(ctl, upper ? &ctl->pvdone : &ctl->pvhalf, (i - 1) & 1, a.status);
             if (!ok) continue;
 #pragma unroll
             for (int c = 0; c < 4; ++c)
@@ -514,7 +525,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             fence_proxy_async_smem();
             tc_fence_before_sync();
             __syncwarp();
-            if (lane == 0) arrive_leader(&ctl->pfull, crank);
+            if (lane == 0) signal_leader(ctl, upper ? &ctl->pfull_b : &ctl->pfull_a, crank, warp == 0 || warp == 2, upper ? 4 : 8);
         }
         // ---- epilogue: row sums, O / l, out (or the split's partial) and lse
         xl[qi * 64 + hl] = l;
@@ -541,7 +552,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 a.part_lse[(static_cast<int64_t>(row) * a.splits + split) * 128 + head] = lse2;
         }
         // stage O * factor as 16-bit rows of 1024 B in the K buffer (the last QK finished with it)
-        const int dbase = (L >= 64 ? 256 : 0) + 128 * h2;
+        const int dbase = (upper ? 256 : 0) + 128 * h2;
         const uint32_t orow = sbase + kOffK + hl * 1024;
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
@@ -577,132 +588,181 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 *reinterpret_cast<uint4*>(dst0 + static_cast<int64_t>(r) * 512 + 8 * k) = x;
             }
         }
-    } else if (warp < kWarpV) {
-        // ======================= K converters =======================
-        const int t = threadIdx.x - 32 * kWarpK;
-        const int j = t >> 2;    // own key of the tile
+    } else if (warp < kWarpQK) {
+        // ============ converters: warps 8-15 K rows of the own keys, warps 16-23 V rows of all keys ============
+        // Each thread stages the bytes it converts itself with cp.async one tile ahead (commit groups in
+        // issue order: part a of tile k, part b of tile k, part a of tile k + 1, ...), so a wait for the
+        // older part leaves the newer one in flight and no arrive of the thread waits for a load.
+        const bool vrole = warp >= kWarpV;
+        const int t = threadIdx.x - 32 * (vrole ? kWarpV : kWarpK);
+        const int j = t >> 2;    // key of the half tile (K: own key j; V: key 64 hv + j)
         const int q = t & 3;     // quarter: blocks 4c + q, RoPE dims 16q..
-        const uint32_t k_s = sbase + kOffK;
-        auto index_of = [&](int i) -> int32_t {
+        const uint32_t fnan = 0x7E007E00u;   // f16 quiet-NaN pairs: a masked key's K row
+        constexpr int sb = R == 352 ? 320 : 256;                 // scale bytes of a record
+        auto index_at = [&](int i, int key) -> int32_t {        // key 0..127 of tile i
             if (i >= n_tiles) return -1;
-            const int pos = key_begin + kTile * i + kOwn * crank + j;
+            const int pos = key_begin + kTile * i + key;
             return pos < key_end ? __ldg(idx_row + pos) : -1;
         };
         auto in_range = [&](int32_t v) { return v >= 0 && static_cast<int64_t>(v) < a.num_slots; };
-        int32_t idx0 = index_of(0), idx1 = index_of(1), idx2 = index_of(2);
-        Raw r;
-        if (in_range(idx0))
-            load_raw<R, kBlkOrder>(a.cache + static_cast<int64_t>(idx0) * R, q, r);
-        else
-            zero_raw(r);
-        if (in_range(idx1)) prefetch_l2(a.cache + static_cast<int64_t>(idx1) * R + (q == 3 ? R - 1 : 128 * q));
-        bool ok = true;
-        for (int i = 0; i < n_tiles && ok; ++i) {
-            const int b = i & 1;
-            const bool valid = in_range(idx0);
-            if (q == 0 && idx0 >= 0 && !valid && a.status != nullptr) atomicOr(a.status, 0x2u);
-            if (i >= 1) ok = wait_warp(ctl, &ctl->qkdone, (i - 1) & 1, a.status);   // K buffer free
-            if (ok && i >= 2) ok = wait_warp(ctl, &ctl->own_empty[b], ((i >> 1) - 1) & 1, a.status);
-            if (ok && i >= 2) ok = wait_warp(ctl, &ctl->peer_empty[b], ((i >> 1) - 1) & 1, a.status);
-            if (!ok) break;
-            // ---- K rows: NoPE blocks (f16) and RoPE (f16 from e4m3, or bf16 verbatim)
-            if (valid) {
-#pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    const __half2 s2 = scale_half2((c < 4 ? r.sc.x >> (8 * c) : r.sc.y >> (8 * (c - 4))) & 0xFFu);
-                    sts_u128(k_s + c * kBlk + swz(j, 2 * q), dq8(r.codes[c].x, s2));
-                    sts_u128(k_s + c * kBlk + swz(j, 2 * q + 1), dq8(r.codes[c].y, s2));
+        bool ok = !aborted(ctl);
+        if (!vrole) {
+            const uint32_t st_a = sbase + kOffStA + j * kStrA;
+            const uint32_t st_b = sbase + kOffStB + j * kStrB<R>;
+            const uint32_t k_s = sbase + kOffK;
+            auto stage_a = [&](int32_t v) {   // codes of blocks 0-15 (bytes 0-127) and the 32 scale bytes
+                if (in_range(v)) {
+                    const uint8_t* rec = a.cache + static_cast<int64_t>(v) * R;
+                    cp_async16(st_a + 16 * q, rec + 16 * q);
+                    cp_async16(st_a + 16 * (q + 4), rec + 16 * (q + 4));
+                    if (q < 2) cp_async16(st_a + 128 + 16 * q, rec + sb + 16 * q);
                 }
-                if constexpr (R == 352) {
-                    const uint2 e0 = e4m3x4_to_f16(r.rope[0].x), e1 = e4m3x4_to_f16(r.rope[0].y);
-                    const uint2 e2 = e4m3x4_to_f16(r.rope[0].z), e3 = e4m3x4_to_f16(r.rope[0].w);
-                    sts_u128(k_s + 8 * kBlk + swz(j, 2 * q), make_uint4(e0.x, e0.y, e1.x, e1.y));
-                    sts_u128(k_s + 8 * kBlk + swz(j, 2 * q + 1), make_uint4(e2.x, e2.y, e3.x, e3.y));
+                cp_async_commit();
+            };
+            auto stage_b = [&](int32_t v) {   // codes of blocks 16-31 (bytes 128-255) and the RoPE bytes
+                if (in_range(v)) {
+                    const uint8_t* rec = a.cache + static_cast<int64_t>(v) * R;
+                    cp_async16(st_b + 16 * q, rec + 128 + 16 * q);
+                    cp_async16(st_b + 16 * (q + 4), rec + 128 + 16 * (q + 4));
+                    cp_async16(st_b + 128 + 16 * q, rec + (R == 352 ? 256 : 304) + 16 * q);
+                    if constexpr (R == 432) cp_async16(st_b + 192 + 16 * q, rec + 304 + 64 + 16 * q);
+                }
+                cp_async_commit();
+            };
+            // the split's index list into L2 (32 indices a line), so that the index loads two tiles
+            // ahead hit L2
+            if (32 * t < key_end - key_begin) prefetch_l2(idx_row + key_begin + 32 * t);
+            const int own = kOwn * crank + j;
+            int32_t idx0 = index_at(0, own), idx1 = index_at(1, own);
+            stage_a(idx0);
+            stage_b(idx0);
+            int32_t idx2 = index_at(2, own);
+            for (int k = 0; k < n_tiles; ++k) {
+                const bool valid = in_range(idx0);
+                if (q == 0 && idx0 >= 0 && !valid && a.status != nullptr) atomicOr(a.status, 0x2u);
+                // ---- blocks 0-3 (dims 0-255) once the previous QK's first half has read them
+                cp_async_wait<1>();
+                __syncwarp();
+                if (k >= 1) ok = wait_warp(ctl, &ctl->khalf, (k - 1) & 1, a.status);
+                if (!ok) break;
+                uint32_t sc_lo, sc_hi;   // byte c: scale of block 4c + q (c = 0..3, 4..7)
+                if constexpr (R == 352 && !kBlkOrder) {
+                    const uint2 s8 = lds_u64(st_a + 128 + 8 * q);   // permuted placement
+                    sc_lo = s8.x;
+                    sc_hi = s8.y;
                 } else {
-                    sts_u128(k_s + 8 * kBlk + swz(j, 2 * q), r.rope[0]);
-                    sts_u128(k_s + 8 * kBlk + swz(j, 2 * q + 1), r.rope[1]);
+                    const uint4 w0 = lds_u128(st_a + 128), w1 = lds_u128(st_a + 144);   // block order
+                    sc_lo = gather_byte4(w0, q);
+                    sc_hi = gather_byte4(w1, q);
                 }
-            } else {
-                // a masked key: quiet-NaN K row, so every score of it is NaN
-                const uint32_t f = 0x7E007E00u;                      // f16 quiet NaN pairs
-                const uint32_t fr = R == 352 ? 0x7E007E00u : 0x7FC07FC0u;   // RoPE block: f16 / bf16
-                const uint4 z = make_uint4(f, f, f, f), zr = make_uint4(fr, fr, fr, fr);
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    sts_u128(k_s + c * kBlk + swz(j, 2 * q), z);
-                    sts_u128(k_s + c * kBlk + swz(j, 2 * q + 1), z);
+                for (int c = 0; c < 4; ++c) {
+                    const uint2 cw = lds_u64(st_a + 32 * c + 8 * q);
+                    const __half2 s2 = scale_half2((sc_lo >> (8 * c)) & 0xFFu);
+                    const uint4 lo = valid ? dq8(cw.x, s2) : make_uint4(fnan, fnan, fnan, fnan);
+                    const uint4 hi = valid ? dq8(cw.y, s2) : make_uint4(fnan, fnan, fnan, fnan);
+                    sts_u128(k_s + c * kBlk + swz(j, 2 * q), lo);
+                    sts_u128(k_s + c * kBlk + swz(j, 2 * q + 1), hi);
                 }
-                sts_u128(k_s + 8 * kBlk + swz(j, 2 * q), zr);
-                sts_u128(k_s + 8 * kBlk + swz(j, 2 * q + 1), zr);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) signal_leader(ctl, &ctl->kfull_a, crank, t == 0, 8);
+                stage_a(idx1);   // the key's four threads have read part a of tile k (the warp synced)
+                // ---- blocks 4-8 (dims 256-575) once the previous QK has finished
+                cp_async_wait<1>();
+                __syncwarp();
+                if (k >= 1) ok = wait_warp(ctl, &ctl->qkdone, (k - 1) & 1, a.status);
+                if (!ok) break;
+#pragma unroll
+                for (int c = 4; c < 8; ++c) {
+                    const uint2 cw = lds_u64(st_b + 32 * (c - 4) + 8 * q);
+                    const __half2 s2 = scale_half2((sc_hi >> (8 * (c - 4))) & 0xFFu);
+                    const uint4 lo = valid ? dq8(cw.x, s2) : make_uint4(fnan, fnan, fnan, fnan);
+                    const uint4 hi = valid ? dq8(cw.y, s2) : make_uint4(fnan, fnan, fnan, fnan);
+                    sts_u128(k_s + c * kBlk + swz(j, 2 * q), lo);
+                    sts_u128(k_s + c * kBlk + swz(j, 2 * q + 1), hi);
+                }
+                if (valid) {
+                    if constexpr (R == 352) {
+                        const uint4 e = lds_u128(st_b + 128 + 16 * q);
+                        const uint2 e0 = e4m3x4_to_f16(e.x), e1 = e4m3x4_to_f16(e.y);
+                        const uint2 e2 = e4m3x4_to_f16(e.z), e3 = e4m3x4_to_f16(e.w);
+                        sts_u128(k_s + 8 * kBlk + swz(j, 2 * q), make_uint4(e0.x, e0.y, e1.x, e1.y));
+                        sts_u128(k_s + 8 * kBlk + swz(j, 2 * q + 1), make_uint4(e2.x, e2.y, e3.x, e3.y));
+                    } else {
+                        sts_u128(k_s + 8 * kBlk + swz(j, 2 * q), lds_u128(st_b + 128 + 32 * q));
+                        sts_u128(k_s + 8 * kBlk + swz(j, 2 * q + 1), lds_u128(st_b + 128 + 32 * q + 16));
+                    }
+                } else {
+                    const uint32_t fr = R == 352 ? fnan : 0x7FC07FC0u;   // RoPE block: f16 / bf16 quiet NaN
+                    sts_u128(k_s + 8 * kBlk + swz(j, 2 * q), make_uint4(fr, fr, fr, fr));
+                    sts_u128(k_s + 8 * kBlk + swz(j, 2 * q + 1), make_uint4(fr, fr, fr, fr));
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) signal_leader(ctl, &ctl->kfull_b, crank, t == 0, 8);
+                stage_b(idx1);
+                idx0 = idx1;
+                idx1 = idx2;
+                idx2 = index_at(k + 3, own);   // in flight until the next tile's first arrive
             }
-            // ---- raw codes of this CTA's dims (local) and of the peer's dims (DSMEM); zeros for a masked key
-            {
-                // codes of blocks 4c + q: c = 0..3 (dims 0-255, CTA 0's half) and c = 4..7 (CTA 1's half)
-                const uint4 z4 = make_uint4(0u, 0u, 0u, 0u);
-                const uint4 lo01 = valid ? make_uint4(r.codes[0].x, r.codes[0].y, r.codes[1].x, r.codes[1].y) : z4;
-                const uint4 lo23 = valid ? make_uint4(r.codes[2].x, r.codes[2].y, r.codes[3].x, r.codes[3].y) : z4;
-                const uint4 hi01 = valid ? make_uint4(r.codes[4].x, r.codes[4].y, r.codes[5].x, r.codes[5].y) : z4;
-                const uint4 hi23 = valid ? make_uint4(r.codes[6].x, r.codes[6].y, r.codes[7].x, r.codes[7].y) : z4;
-                const uint32_t slo = valid ? r.sc.x : 0u, shi = valid ? r.sc.y : 0u;
-                const uint32_t own_buf = sbase + kOffOwnRaw + b * kRawBytes;
-                sts_u128(raw_codes_at(own_buf, j, q), crank == 0 ? lo01 : hi01);
-                sts_u128(raw_codes_at(own_buf, j, q) + 16, crank == 0 ? lo23 : hi23);
-                asm volatile("st.shared.u32 [%0], %1;" ::"r"(raw_scale_at(own_buf, j, q)), "r"(crank == 0 ? slo : shi)
-                             : "memory");
-                const uint32_t peer_buf = mapa_shared(sbase + kOffPeerRaw + b * kRawBytes, 1 - crank);
-                const uint32_t peer_bar = mapa_shared(smem_addr(&ctl->peer_full[b]), 1 - crank);
-                st_async_u4(raw_codes_at(peer_buf, j, q), crank == 0 ? hi01 : lo01, peer_bar);
-                st_async_u4(raw_codes_at(peer_buf, j, q) + 16, crank == 0 ? hi23 : lo23, peer_bar);
-                st_async_b32(raw_scale_at(peer_buf, j, q), crank == 0 ? shi : slo, peer_bar);
+        } else {
+            const uint32_t v_s = sbase + kOffV;
+            auto stage_v = [&](int hv, int32_t v) {   // this CTA's half of the codes and its 16 scale bytes
+                const uint32_t st = sbase + kOffStV<R> + (hv * kOwn + j) * kStrV<R>;
+                if (in_range(v)) {
+                    const uint8_t* rec = a.cache + static_cast<int64_t>(v) * R;
+                    cp_async16(st + 16 * q, rec + 128 * crank + 16 * q);
+                    cp_async16(st + 16 * (q + 4), rec + 128 * crank + 16 * (q + 4));
+                    if constexpr (R == 352 && !kBlkOrder)
+                        cp_async4(st + 128 + 4 * q, rec + 320 + 8 * q + 4 * crank);   // blocks 4c + q, c in half
+                    else if (q == 0)
+                        cp_async16(st + 128, rec + sb + 16 * crank);   // blocks 16 crank ..
+                }
+                cp_async_commit();
+            };
+            int32_t ia0 = index_at(0, j), ib0 = index_at(0, kOwn + j);
+            int32_t ia1 = index_at(1, j), ib1 = index_at(1, kOwn + j);
+            stage_v(0, ia0);
+            stage_v(1, ib0);
+            int32_t ia2 = index_at(2, j), ib2 = index_at(2, kOwn + j);
+            for (int k = 0; k < n_tiles; ++k) {
+#pragma unroll
+                for (int hv = 0; hv < 2; ++hv) {   // V rows 64 hv + j: CTA hv's keys
+                    cp_async_wait<1>();
+                    __syncwarp();
+                    if (k == 0 && hv == 0) ok = wait_warp(ctl, &ctl->qstaged, 0, a.status);   // the V buffer held q
+                    if (ok && k >= 1) ok = wait_warp(ctl, hv == 0 ? &ctl->pvhalf : &ctl->pvdone, (k - 1) & 1, a.status);
+                    if (!ok) break;
+                    const uint32_t st = sbase + kOffStV<R> + (hv * kOwn + j) * kStrV<R>;
+                    const bool valid = in_range(hv == 0 ? ia0 : ib0);
+                    uint32_t sbytes;   // byte cl: scale of block 4 (4 crank + cl) + q
+                    if constexpr (R == 352 && !kBlkOrder)
+                        sbytes = lds_u32(st + 128 + 4 * q);
+                    else
+                        sbytes = gather_byte4(lds_u128(st + 128), q);
+                    const uint2 c0 = lds_u64(st + 8 * q), c1 = lds_u64(st + 32 + 8 * q);
+                    const uint2 c2 = lds_u64(st + 64 + 8 * q), c3 = lds_u64(st + 96 + 8 * q);
+                    // a masked key's V row is zero (its probability is zero, and 0 x 0 stays 0)
+                    write_v(v_s, 64 * hv + j, q,
+                            valid ? make_uint4(c0.x, c0.y, c1.x, c1.y) : make_uint4(0u, 0u, 0u, 0u),
+                            valid ? make_uint4(c2.x, c2.y, c3.x, c3.y) : make_uint4(0u, 0u, 0u, 0u),
+                            valid ? sbytes : 0u);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) signal_leader(ctl, hv == 0 ? &ctl->vfull_a : &ctl->vfull_b, crank, t == 0, 8);
+                    stage_v(hv, hv == 0 ? ia1 : ib1);
+                }
+                if (!ok) break;
+                ia0 = ia1;
+                ib0 = ib1;
+                ia1 = ia2;
+                ib1 = ib2;
+                ia2 = index_at(k + 3, j);
+                ib2 = index_at(k + 3, kOwn + j);
             }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-                arrive_leader(&ctl->kfull, crank);
-                mbar_arrive(&ctl->own_full[b]);
-            }
-            // ---- next tile's record into registers (L2-prefetched a tile ago), prefetch the one after
-            idx0 = idx1;
-            idx1 = idx2;
-            idx2 = index_of(i + 3);
-            if (in_range(idx0))
-                load_raw<R, kBlkOrder>(a.cache + static_cast<int64_t>(idx0) * R, q, r);
-            else
-                zero_raw(r);
-            if (in_range(idx1)) prefetch_l2(a.cache + static_cast<int64_t>(idx1) * R + (q == 3 ? R - 1 : 128 * q));
         }
-    } else if (warp < kWarpQK) {
-        // ======================= V converters =======================
-        const int t = threadIdx.x - 32 * kWarpV;
-        const int j = t >> 2;
-        const int q = t & 3;
-        const uint32_t v_s = sbase + kOffV;
-        const int row_own = kOwn * crank + j;
-        const int row_peer = kOwn * (1 - crank) + j;
-        bool ok = true;
-        for (int i = 0; i < n_tiles && ok; ++i) {
-            const int b = i & 1;
-            if (i == 0) ok = wait_warp(ctl, &ctl->qstaged, 0, a.status);   // the V buffer held q
-            if (ok && i >= 1) ok = wait_warp(ctl, &ctl->pvdone, (i - 1) & 1, a.status);
-            if (ok) ok = wait_warp(ctl, &ctl->own_full[b], (i >> 1) & 1, a.status);
-            if (ok) ok = wait_warp(ctl, &ctl->peer_full[b], (i >> 1) & 1, a.status);
-            if (!ok) break;
-            const uint32_t own_buf = sbase + kOffOwnRaw + b * kRawBytes;
-            const uint32_t peer_buf = sbase + kOffPeerRaw + b * kRawBytes;
-            write_v(v_s, row_own, q, lds_u128(raw_codes_at(own_buf, j, q)), lds_u128(raw_codes_at(own_buf, j, q) + 16),
-                    lds_u32(raw_scale_at(own_buf, j, q)));
-            write_v(v_s, row_peer, q, lds_u128(raw_codes_at(peer_buf, j, q)),
-                    lds_u128(raw_codes_at(peer_buf, j, q) + 16), lds_u32(raw_scale_at(peer_buf, j, q)));
-            fence_proxy_async_smem();
-            // the peer may send tile i + 2 into this buffer once it is armed again and released
-            if (t == 0 && i + 2 < n_tiles) mbar_arrive_expect_tx(&ctl->peer_full[b], kRawBytes);
-            __syncwarp();
-            if (lane == 0) {
-                arrive_leader(&ctl->vfull, crank);
-                mbar_arrive(&ctl->own_empty[b]);
-                mbar_arrive_cluster(mapa_shared(smem_addr(&ctl->peer_empty[b]), 1 - crank));
-            }
-        }
+        cp_async_wait<0>();   // no copy into shared memory outlives the loop
     } else if (warp == kWarpQK) {
         // ======================= QK issuer (CTA 0) =======================
         if (crank == 0) {
@@ -711,19 +771,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const uint64_t kdesc0 = sdesc_sw128(sbase + kOffK, 16, 1024);
             const uint64_t qdesc0 = sdesc_sw128(sbase + kOffQs, 16, 1024);
             const bool leader = elect_one_in_warp();
-            bool ok = wait_warp(ctl, &ctl->qready, 0, a.status);
+            bool ok = wait_peer(ctl, &ctl->qready, 0, a.status);
             for (int i = 0; i < n_tiles && ok; ++i) {
-                ok = wait_warp(ctl, &ctl->kfull, i & 1, a.status);
-                if (ok && i >= 1) ok = wait_warp(ctl, &ctl->sfree, (i - 1) & 1, a.status);
+                ok = wait_peer(ctl, &ctl->kfull_a, i & 1, a.status);
+                if (ok && i >= 1) ok = wait_peer(ctl, &ctl->sfree, (i - 1) & 1, a.status);
+                if (!ok) break;
+                tc_fence_after_sync();
+                const uint32_t d = tmem + kColS;
+                if (leader) {
+#pragma unroll
+                    for (int kk = 0; kk < 16; ++kk)   // dims 0-255: q from tensor memory
+                        mma_ts_cg2(d, tmem + kColQ + 8 * kk,
+                                   kdesc0 + static_cast<uint64_t>(((kk >> 2) * kBlk + (kk & 3) * 32) >> 4), idesc_f16,
+                                   kk > 0 ? 1u : 0u);
+                    mma_commit_cg2(&ctl->khalf, 0x3);
+                }
+                __syncwarp();
+                ok = wait_peer(ctl, &ctl->kfull_b, i & 1, a.status);
                 if (!ok) break;
                 tc_fence_after_sync();
                 if (leader) {
-                    const uint32_t d = tmem + kColS;
 #pragma unroll
-                    for (int kk = 0; kk < 36; ++kk) {
+                    for (int kk = 16; kk < 36; ++kk) {
                         const uint64_t kd = kdesc0 + static_cast<uint64_t>(((kk >> 2) * kBlk + (kk & 3) * 32) >> 4);
                         if (kk < kQTmemSteps)
-                            mma_ts_cg2(d, tmem + kColQ + 8 * kk, kd, idesc_f16, kk > 0 ? 1u : 0u);
+                            mma_ts_cg2(d, tmem + kColQ + 8 * kk, kd, idesc_f16, 1u);
                         else
                             mma_ss_cg2(d, qdesc0 + static_cast<uint64_t>((((kk - 24) >> 2) * kBlk + (kk & 3) * 32) >> 4),
                                        kd, kk >= 32 ? idesc_rope : idesc_f16, 1u);
@@ -744,23 +816,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const bool leader = elect_one_in_warp();
             bool ok = true;
             for (int i = 0; i < n_tiles && ok; ++i) {
-                ok = wait_warp(ctl, &ctl->vfull, i & 1, a.status);
-                if (ok) ok = wait_warp(ctl, &ctl->pfull, i & 1, a.status);
-                if (!ok) break;
-                tc_fence_after_sync();
-                if (leader) {
 #pragma unroll
-                    for (int ks = 0; ks < kTile / 16; ++ks) {
-                        const uint64_t pd = pdesc0 + static_cast<uint64_t>(((ks >> 2) * kBlk + (ks & 3) * 32) >> 4);
+                for (int hv = 0; hv < 2; ++hv) {   // keys 0-63, then keys 64-127
+                    ok = wait_peer(ctl, hv == 0 ? &ctl->vfull_a : &ctl->vfull_b, i & 1, a.status);
+                    if (ok) ok = wait_peer(ctl, hv == 0 ? &ctl->pfull_a : &ctl->pfull_b, i & 1, a.status);
+                    if (!ok) break;
+                    tc_fence_after_sync();
+                    if (leader) {
 #pragma unroll
-                        for (int jj = 0; jj < 2; ++jj)
-                            mma_ss_cg2(tmem + kColO + 128 * jj, pd,
-                                       vdesc0 + static_cast<uint64_t>((2 * jj * kVBlk + ks * 2048) >> 4), idesc_pv,
-                                       (i > 0 || ks > 0) ? 1u : 0u);
+                        for (int ks = 4 * hv; ks < 4 * hv + 4; ++ks) {
+                            const uint64_t pd = pdesc0 + static_cast<uint64_t>(((ks >> 2) * kBlk + (ks & 3) * 32) >> 4);
+#pragma unroll
+                            for (int jj = 0; jj < 2; ++jj)
+                                mma_ss_cg2(tmem + kColO + 128 * jj, pd,
+                                           vdesc0 + static_cast<uint64_t>((2 * jj * kVBlk + ks * 2048) >> 4), idesc_pv,
+                                           (i > 0 || ks > 0) ? 1u : 0u);
+                        }
+                        mma_commit_cg2(hv == 0 ? &ctl->pvhalf : &ctl->pvdone, 0x3);
                     }
-                    mma_commit_cg2(&ctl->pvdone, 0x3);
+                    __syncwarp();
                 }
-                __syncwarp();
             }
             if (leader) mma_commit_cg2(&ctl->drain, 0x1);
             __syncwarp();
@@ -816,7 +891,7 @@ cudaError_t prepare_kernel() {
     if (err != cudaSuccess) return err;
     const uint64_t bit = dev < 64 ? (uint64_t(1) << dev) : 0;
     if (bit != 0 && (done.load(std::memory_order_relaxed) & bit)) return cudaSuccess;
-    err = cudaFuncSetAttribute(decode_pair_kernel<R, kBlkOrder>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
+    err = cudaFuncSetAttribute(decode_pair_kernel<R, kBlkOrder>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc<R>);
     if (err == cudaSuccess && bit != 0) done.fetch_or(bit, std::memory_order_relaxed);
     return err;
 }
@@ -858,7 +933,7 @@ cudaError_t launch_decode_pair(const DecodeArgs& d, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(d.rows) * static_cast<unsigned>(d.splits) * 2u);
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = kSmemAlloc;
+    cfg.dynamicSmemBytes = d.record_bytes == 432 ? kSmemAlloc<432> : kSmemAlloc<352>;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // see griddepcontrol.wait
