@@ -1028,8 +1028,19 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
     const int row = rh / h_q;
     const int h = rh % h_q;
     const int64_t base = static_cast<int64_t>(row) * splits;
+    // every load of the first four splits goes out before any result is used: one memory round trip
+    const float sk = sink != nullptr ? __ldg(sink + h) : 0.0f;
     const float v0 = lane < splits ? part_lse[(base + lane) * h_q + h] : -INFINITY;
     const float v1 = lane + 32 < splits ? part_lse[(base + lane + 32) * h_q + h] : -INFINITY;
+    constexpr int kEarly = 4;
+    uint2 early[kEarly][4];
+#pragma unroll
+    for (int sp = 0; sp < kEarly; ++sp) {
+        const uint16_t* src = part_out + ((base + sp) * h_q + h) * 512 + 4 * lane;
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            early[sp][k] = sp < splits ? __ldg(reinterpret_cast<const uint2*>(src + 128 * k)) : make_uint2(0u, 0u);
+    }
     float m = fmaxf(v0, v1);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
@@ -1043,21 +1054,31 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
         total = (m + log2f(sum)) * kLn2;
-        const float inv = 1.0f / (sum + (sink != nullptr ? exp2f(__ldg(sink + h) * kLog2e - m) : 0.0f));
+        const float inv = 1.0f / (sum + (sink != nullptr ? exp2f(sk * kLog2e - m) : 0.0f));
         const float w0 = e0 * inv, w1 = e1 * inv;
-        for (int sp = 0; sp < splits; ++sp) {
-            const float w = __shfl_sync(0xffffffffu, sp < 32 ? w0 : w1, sp & 31);
-            const uint16_t* src = part_out + ((base + sp) * h_q + h) * 512 + 4 * lane;
+        auto accumulate = [&](float w, const uint2 (&u)[4]) {
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-                const uint2 u = *reinterpret_cast<const uint2*>(src + 128 * k);   // four f16
-                const float2 lo = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
-                const float2 hi = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
+                const float2 lo = __half22float2(*reinterpret_cast<const __half2*>(&u[k].x));
+                const float2 hi = __half22float2(*reinterpret_cast<const __half2*>(&u[k].y));
                 acc[k].x += w * lo.x;
                 acc[k].y += w * lo.y;
                 acc[k].z += w * hi.x;
                 acc[k].w += w * hi.y;
             }
+        };
+#pragma unroll
+        for (int sp = 0; sp < kEarly; ++sp) {
+            const float w = __shfl_sync(0xffffffffu, w0, sp);
+            if (sp < splits) accumulate(w, early[sp]);
+        }
+        for (int sp = kEarly; sp < splits; ++sp) {
+            const float w = __shfl_sync(0xffffffffu, sp < 32 ? w0 : w1, sp & 31);
+            const uint16_t* src = part_out + ((base + sp) * h_q + h) * 512 + 4 * lane;
+            uint2 u[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) u[k] = __ldg(reinterpret_cast<const uint2*>(src + 128 * k));
+            accumulate(w, u);
         }
     }
     __nv_bfloat16* dst = out + static_cast<int64_t>(rh) * 512 + 4 * lane;
@@ -1163,8 +1184,9 @@ cudaError_t launch_wait_timeout_probe(uint32_t* status, uint64_t* elapsed_ns, cu
 
 cudaError_t launch_sparse_decode(const DecodeArgs& d, cudaStream_t stream) {
     cudaError_t err;
+    bool merged = false;   // the decode grid merged the splits itself
     if (decode_pair_supported(d)) {
-        err = launch_decode_pair(d, stream);
+        err = launch_decode_pair(d, stream, &merged);
     } else {
         KernelArgs a;
         if (!encode_cache_map(&a.tmap, d.cache, d.num_slots, d.record_bytes)) return cudaErrorInvalidValue;
@@ -1210,12 +1232,17 @@ cudaError_t launch_sparse_decode(const DecodeArgs& d, cudaStream_t stream) {
         err = cudaLaunchKernelEx(&cfg, kernel, a);
         if (err == cudaSuccess) err = cudaGetLastError();
     }
-    if (err != cudaSuccess || d.splits == 1) return err;
+    if (err != cudaSuccess || d.splits == 1 || merged) return err;
     return launch_split_merge(d, stream);
 }
 
-// The merge launches while the decode grid runs and waits for it on the device.
+// The merge launches while the decode grid runs and waits for it on the device. It asks for the
+// same shared-memory carveout as the decode kernels, so that the SMs need not repartition their
+// L1 and shared memory between the two grids.
 cudaError_t launch_split_merge(const DecodeArgs& d, cudaStream_t stream) {
+    static const cudaError_t carveout =
+        cudaFuncSetAttribute(combine_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+    if (carveout != cudaSuccess) return carveout;
     cudaLaunchConfig_t cfg = {};
     const int rows_heads = d.rows * d.h_q;
     cfg.gridDim = dim3(static_cast<unsigned>((rows_heads + 7) / 8));

@@ -143,6 +143,8 @@ struct KernelArgs {
     uint16_t* part_out;       // f16 partial outputs [rows, splits, 128, 512]
     float* part_lse;          // log2 domain
     uint32_t* status;
+    int merge;                // 1: the row's splits share a cluster (pair p = ranks 2p, 2p + 1) and pair 0
+                              // merges their partials into out and lse after the whole cluster is done
 };
 
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t threads) {
@@ -184,13 +186,14 @@ __device__ __forceinline__ bool wait_peer(Ctl* ctl, uint64_t* bar, uint32_t pari
 // wait until its earlier writes are visible across the cluster, as a remote release arrive would
 // (the complete_tx carries release semantics at cluster scope).
 __device__ __forceinline__ void signal_leader(Ctl* ctl, uint64_t* bar, int crank, bool arm, uint32_t n_peer) {
+    const uint32_t leader = cluster_ctarank() & ~1u;   // the pair's first CTA
     if (crank == 0) {
         if (arm)
             mbar_arrive_expect_tx(bar, 4u * n_peer);
         else
             mbar_arrive(bar);
     } else {
-        st_async_b32(mapa_shared(smem_addr(&ctl->sig_sink), 0), 0u, mapa_shared(smem_addr(bar), 0));
+        st_async_b32(mapa_shared(smem_addr(&ctl->sig_sink), leader), 0u, mapa_shared(smem_addr(bar), leader));
     }
 }
 
@@ -260,15 +263,85 @@ __device__ __forceinline__ void write_v(uint32_t v_s, int row, int q, const uint
 
 // kBlkOrder: the 32 scale bytes are in block order (432-byte records, and the 352-byte record of
 // the scale-layout comparison) instead of the permuted placement 8 (s & 3) + (s >> 2).
+// The row's split merge, by every CTA of its cluster once every split's partial is written: the
+// cluster's 2S CTAs x 26 warps take the 128 heads in turn (warp-sized work items), lane l dims
+// 16l .. 16l + 15.
+//   out = sum_s w_s part_s,  w_s = 2^{lse2_s} / (sum_s 2^{lse2_s} + e^{sink}),  lse = ln sum_s e^{lse_s}
+// (lse2 = log2-domain partial lse; the sink is not part of lse). Every load of a head goes out before
+// any is used.
+constexpr int kMaxClusterSplits = 4;   // a cluster holds at most 8 CTAs
+
+__device__ __forceinline__ void merge_splits(const KernelArgs& a, int row) {
+    const int lane = threadIdx.x & 31;
+    const int64_t rbase = static_cast<int64_t>(row) * a.splits;
+    const int workers = 2 * a.splits * (kThreads / 32);
+    const int me = static_cast<int>(cluster_ctarank()) * (kThreads / 32) + (threadIdx.x >> 5);
+#pragma unroll 1
+    for (int head = me; head < 128; head += workers) {
+        float v[kMaxClusterSplits];
+        uint4 d0[kMaxClusterSplits], d1[kMaxClusterSplits];
+        const float sk = a.sink != nullptr ? __ldg(a.sink + head) : 0.0f;
+#pragma unroll
+        for (int sp = 0; sp < kMaxClusterSplits; ++sp) {
+            v[sp] = -INFINITY;
+            d0[sp] = d1[sp] = make_uint4(0u, 0u, 0u, 0u);
+            if (sp < a.splits) {
+                v[sp] = __ldcg(a.part_lse + (rbase + sp) * 128 + head);
+                const uint4* src = reinterpret_cast<const uint4*>(a.part_out + ((rbase + sp) * 128 + head) * 512 + 16 * lane);
+                d0[sp] = __ldcg(src);
+                d1[sp] = __ldcg(src + 1);
+            }
+        }
+        float m = v[0];
+#pragma unroll
+        for (int sp = 1; sp < kMaxClusterSplits; ++sp) m = fmaxf(m, v[sp]);
+        float acc[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) acc[e] = 0.0f;
+        float total = -INFINITY;
+        if (m != -INFINITY) {
+            float ex[kMaxClusterSplits];
+            float sum = 0.0f;
+#pragma unroll
+            for (int sp = 0; sp < kMaxClusterSplits; ++sp) {
+                ex[sp] = exp2f(v[sp] - m);
+                sum += ex[sp];
+            }
+            total = (m + log2f(sum)) * kLn2;
+            const float inv = 1.0f / (sum + (a.sink != nullptr ? exp2f(sk * kLog2e - m) : 0.0f));
+#pragma unroll
+            for (int sp = 0; sp < kMaxClusterSplits; ++sp) {
+                const float w = ex[sp] * inv;
+                const uint32_t hw[8] = {d0[sp].x, d0[sp].y, d0[sp].z, d0[sp].w, d1[sp].x, d1[sp].y, d1[sp].z, d1[sp].w};
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hw[e]));
+                    acc[2 * e] += w * f.x;
+                    acc[2 * e + 1] += w * f.y;
+                }
+            }
+        }
+        uint4* dst = reinterpret_cast<uint4*>(a.out + (static_cast<int64_t>(row) * 128 + head) * 512 + 16 * lane);
+        dst[0] = make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]), pack_bf16x2(acc[4], acc[5]),
+                            pack_bf16x2(acc[6], acc[7]));
+        dst[1] = make_uint4(pack_bf16x2(acc[8], acc[9]), pack_bf16x2(acc[10], acc[11]), pack_bf16x2(acc[12], acc[13]),
+                            pack_bf16x2(acc[14], acc[15]));
+        if (lane == 0) a.lse[static_cast<int64_t>(row) * 128 + head] = total;
+    }
+}
+
+// Launched in clusters of two CTAs per split pair (one pair, or all splits of a row when they merge
+// in the kernel).
 template <int R, bool kBlkOrder>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 1)
     decode_pair_kernel(const __grid_constant__ KernelArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     Ctl* ctl = reinterpret_cast<Ctl*>(smem);
     const uint32_t sbase = smem_addr(smem);
 
-    const int crank = static_cast<int>(cluster_ctarank());
+    const int crank = static_cast<int>(cluster_ctarank() & 1u);   // CTA within the pair
+    const int pb = static_cast<int>(cluster_ctarank() & ~1u);     // the pair's first rank in the cluster
     const int pair = blockIdx.x >> 1;
     const int split = pair % a.splits;
     const int row = pair / a.splits;
@@ -784,7 +857,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         mma_ts_cg2(d, tmem + kColQ + 8 * kk,
                                    kdesc0 + static_cast<uint64_t>(((kk >> 2) * kBlk + (kk & 3) * 32) >> 4), idesc_f16,
                                    kk > 0 ? 1u : 0u);
-                    mma_commit_cg2(&ctl->khalf, 0x3);
+                    mma_commit_cg2(&ctl->khalf, 0x3u << pb);
                 }
                 __syncwarp();
                 ok = wait_peer(ctl, &ctl->kfull_b, i & 1, a.status);
@@ -800,11 +873,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                             mma_ss_cg2(d, qdesc0 + static_cast<uint64_t>((((kk - 24) >> 2) * kBlk + (kk & 3) * 32) >> 4),
                                        kd, kk >= 32 ? idesc_rope : idesc_f16, 1u);
                     }
-                    mma_commit_cg2(&ctl->qkdone, 0x3);
+                    mma_commit_cg2(&ctl->qkdone, 0x3u << pb);
                 }
                 __syncwarp();
             }
-            if (leader) mma_commit_cg2(&ctl->drain, 0x1);
+            if (leader) mma_commit_cg2(&ctl->drain, 0x1u << pb);
             __syncwarp();
         }
     } else {
@@ -832,12 +905,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                            vdesc0 + static_cast<uint64_t>((2 * jj * kVBlk + ks * 2048) >> 4), idesc_pv,
                                            (i > 0 || ks > 0) ? 1u : 0u);
                         }
-                        mma_commit_cg2(hv == 0 ? &ctl->pvhalf : &ctl->pvdone, 0x3);
+                        mma_commit_cg2(hv == 0 ? &ctl->pvhalf : &ctl->pvdone, 0x3u << pb);
                     }
                     __syncwarp();
                 }
             }
-            if (leader) mma_commit_cg2(&ctl->drain, 0x1);
+            if (leader) mma_commit_cg2(&ctl->drain, 0x1u << pb);
             __syncwarp();
         }
     }
@@ -847,11 +920,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (!mbar_wait(&ctl->drain, 0)) set_abort(ctl, a.status);
     }
     tc_fence_before_sync();
-    cluster_sync();   // no CTA leaves while its peer may still write its shared or tensor memory
+    // No CTA leaves while its peer may still write its shared or tensor memory; with a merge, every
+    // split's partial is also written (release / acquire at cluster scope) once this returns.
+    cluster_sync();
     if (warp == kWarpQK) {
         tc_fence_after_sync();
         tmem_dealloc_cg2(tmem, kTmemCols);
     }
+    if (a.merge) merge_splits(a, row);
 }
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -906,7 +982,7 @@ int decode_pair_keys_per_split(int topk, int splits) {
     return (per + pairdec::kTile - 1) / pairdec::kTile * pairdec::kTile;
 }
 
-cudaError_t launch_decode_pair(const DecodeArgs& d, cudaStream_t stream) {
+cudaError_t launch_decode_pair(const DecodeArgs& d, cudaStream_t stream, bool* merged) {
     using namespace pairdec;
     KernelArgs a;
     if (!encode_q_map(&a.qmap, d.q, static_cast<int64_t>(d.rows) * 128)) return cudaErrorInvalidValue;
@@ -935,11 +1011,42 @@ cudaError_t launch_decode_pair(const DecodeArgs& d, cudaStream_t stream) {
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = d.record_bytes == 432 ? kSmemAlloc<432> : kSmemAlloc<352>;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // see griddepcontrol.wait
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
+    // All splits of a row in one cluster when there are 2-4 of them and such clusters fit on this
+    // GPU: the kernel then merges them itself and no merge grid follows.
+    a.merge = 0;
+    if (d.splits >= 2 && d.splits <= kMaxClusterSplits) {
+        attr[1].val.clusterDim.x = 2u * static_cast<unsigned>(d.splits);
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        // how many such clusters fit at once, asked once per kernel variant, cluster size and device
+        static std::atomic<int> fits[3][kMaxClusterSplits + 1][8];
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidValue;
+        const int variant = d.record_bytes == 432 ? 2 : d.block_scales ? 1 : 0;
+        std::atomic<int>& known = fits[variant][d.splits][dev & 7];
+        int state = known.load(std::memory_order_relaxed);   // 0 unknown, 1 none fits, else 2 + clusters that fit
+        if (state == 0) {
+            int clusters = 0;
+            state = cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg) == cudaSuccess && clusters > 0 ? clusters + 2 : 1;
+            (void)cudaGetLastError();
+            known.store(state, std::memory_order_relaxed);
+        }
+        // and only when the whole grid is resident at once (a second wave of large clusters would
+        // leave SMs idle)
+        a.merge = state >= 2 && static_cast<int64_t>(state - 2) >= d.rows ? 1 : 0;
+    }
+    if (!a.merge) {
+        attr[1].val.clusterDim.x = 2;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+    }
+    *merged = a.merge != 0;
     err = cudaLaunchKernelEx(&cfg, kernel, a);
     if (err == cudaSuccess) err = cudaGetLastError();
     return err;
