@@ -173,8 +173,13 @@ NVFP4_MLA_API int nvfp4_sparse_mla_decode(const void* q, const uint8_t* cache, i
  *  - A problem whose split count (num_splits, or the library's choice when 0) needs more
  *    scratch than that returns NVFP4_MLA_ERR_WORKSPACE and launches nothing; pass a smaller
  *    num_splits (1 needs no scratch).
- *  - The first call on each device looks up the array's device address with that device
- *    current and caches it; make that first call before any stream capture.
+ *  - A call outside stream capture looks up the array's device address with the device
+ *    current and keeps it; a call under capture uses the kept address. So make one call
+ *    before any capture, and make one again after cudaDeviceReset or any other reset of the
+ *    device's primary context: the reset may move the array, and an address kept from before
+ *    it is invalid until an uncaptured call looks the array up again.
+ *  - Argument checks come first and match nvfp4_sparse_mla_decode's (same status for the same
+ *    bad argument); a failed runtime query leaves no pending CUDA error behind.
  *  - All calls share the array and it keeps the last call's contents (nothing in it needs to
  *    start at zero: each call writes every value it reads). Calls whose kernels may overlap on
  *    the GPU, e.g. on unordered streams, race on it and must be serialized by the caller.

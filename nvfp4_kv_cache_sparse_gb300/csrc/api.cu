@@ -89,6 +89,30 @@ int check_decode_shape(int32_t batch, int32_t s_q, int32_t h_q, int32_t topk, in
 
 }  // namespace
 
+namespace nvfp4mla {
+
+int check_decode_call(const void* q, const uint8_t* cache, int64_t num_slots, int32_t record_bytes,
+                      const int32_t* indices, int32_t batch, int32_t s_q, int32_t h_q, int32_t topk,
+                      const float* attn_sink, const void* out, const float* lse, int32_t num_splits, int64_t* rows,
+                      int* sms) {
+    *rows = 0;
+    *sms = 0;
+    const int st = check_decode_shape(batch, s_q, h_q, topk, record_bytes, num_splits);
+    if (st != NVFP4_MLA_OK) return st;
+    if (num_slots < 0) return NVFP4_MLA_ERR_INVALID_ARG;
+    *rows = static_cast<int64_t>(batch) * s_q;
+    if (*rows == 0) return NVFP4_MLA_OK;
+    if (!q || !cache || !indices || !out || !lse) return NVFP4_MLA_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(cache, 16) || !aligned(out, 16) || !aligned(indices, 4) || !aligned(lse, 4))
+        return NVFP4_MLA_ERR_INVALID_ARG;
+    if (attn_sink && !aligned(attn_sink, 4)) return NVFP4_MLA_ERR_INVALID_ARG;
+    int status = NVFP4_MLA_OK;
+    *sms = device_sm_count(&status);
+    return *sms > 0 ? NVFP4_MLA_OK : status;
+}
+
+}  // namespace nvfp4mla
+
 extern "C" {
 
 NVFP4_MLA_API int nvfp4_mla_quantize_append(const void* kv_latent, int64_t latent_row_stride, const void* k_rope,
@@ -135,18 +159,11 @@ NVFP4_MLA_API int nvfp4_sparse_mla_decode(const void* q, const uint8_t* cache, i
                                           int32_t topk, float sm_scale, const float* attn_sink, void* out, float* lse,
                                           int32_t num_splits, void* workspace, size_t workspace_bytes,
                                           uint32_t* dev_status, void* stream) {
-    const int st = check_decode_shape(batch, s_q, h_q, topk, record_bytes, num_splits);
-    if (st != NVFP4_MLA_OK) return st;
-    if (num_slots < 0) return NVFP4_MLA_ERR_INVALID_ARG;
-    const int64_t rows = static_cast<int64_t>(batch) * s_q;
-    if (rows == 0) return NVFP4_MLA_OK;
-    if (!q || !cache || !indices || !out || !lse) return NVFP4_MLA_ERR_INVALID_ARG;
-    if (!aligned(q, 16) || !aligned(cache, 16) || !aligned(out, 16) || !aligned(indices, 4) || !aligned(lse, 4))
-        return NVFP4_MLA_ERR_INVALID_ARG;
-    if (attn_sink && !aligned(attn_sink, 4)) return NVFP4_MLA_ERR_INVALID_ARG;
-    int status = NVFP4_MLA_OK;
-    const int sms = device_sm_count(&status);
-    if (sms <= 0) return status;
+    int64_t rows = 0;
+    int sms = 0;
+    const int st = nvfp4mla::check_decode_call(q, cache, num_slots, record_bytes, indices, batch, s_q, h_q, topk,
+                                               attn_sink, out, lse, num_splits, &rows, &sms);
+    if (st != NVFP4_MLA_OK || rows == 0) return st;
     const int splits = num_splits > 0 ? num_splits : auto_splits(rows, topk, sms);
     const size_t need = workspace_for(rows, h_q, splits);
     if (need > 0 && (!workspace || workspace_bytes < need || !aligned(workspace, 256))) return NVFP4_MLA_ERR_WORKSPACE;

@@ -16,9 +16,12 @@
 //  * All calls share the array and it keeps what the last call wrote. Nothing in it has to
 //    start at zero: each call writes every partial value it later reads. Two calls whose
 //    kernels overlap on the GPU (different streams, no ordering) race on it.
-//  * The host cannot use the array's name as a device address. The first call on each device
-//    asks the runtime for that address (cudaGetSymbolAddress, with the device current) and
-//    caches it; make that first call before any stream capture.
+//  * The host cannot use the array's name as a device address. A call outside stream capture
+//    asks the runtime for it (cudaGetSymbolAddress, with the device current) and keeps it for
+//    the device; a call under capture uses the one kept, so make one call before any capture,
+//    and again after a device or primary-context reset (cudaDeviceReset), which may move the array.
+//  * Every host-side check of the workspace entry point runs first, so a call with a bad
+//    argument returns the same status as that entry point and asks the runtime for nothing.
 //  * No cudaMalloc, cudaFree or allocating library routine is called.
 #include <cuda_runtime.h>
 
@@ -26,6 +29,7 @@
 #include <mutex>
 
 #include "../../include/nvfp4_mla.h"
+#include "launch.h"
 
 namespace {
 
@@ -37,15 +41,27 @@ static __device__ __align__(256) unsigned char g_decode_scratch[kNoAllocScratchB
 std::mutex g_setup_mutex;
 void* g_scratch_ptr[kMaxDevices] = {};
 
-// Device address of g_decode_scratch on the current device (set up once per device).
-int scratch_address(void** out) {
+// Device address of g_decode_scratch on the current device: looked up again on every call outside
+// stream capture, the kept one under capture. A failed runtime call leaves no error pending.
+int scratch_address(cudaStream_t stream, void** out) {
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return NVFP4_MLA_ERR_CUDA;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return NVFP4_MLA_ERR_CUDA;
+    }
     if (dev < 0 || dev >= kMaxDevices) return NVFP4_MLA_ERR_UNSUPPORTED;
+    cudaStreamCaptureStatus capture = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &capture) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return NVFP4_MLA_ERR_CUDA;
+    }
     std::lock_guard<std::mutex> lock(g_setup_mutex);
-    if (g_scratch_ptr[dev] == nullptr) {
+    if (capture == cudaStreamCaptureStatusNone || g_scratch_ptr[dev] == nullptr) {
         void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess || p == nullptr) return NVFP4_MLA_ERR_CUDA;
+        if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess || p == nullptr) {
+            (void)cudaGetLastError();
+            return NVFP4_MLA_ERR_CUDA;
+        }
         g_scratch_ptr[dev] = p;
     }
     *out = g_scratch_ptr[dev];
@@ -58,13 +74,18 @@ extern "C" NVFP4_MLA_API int nvfp4_sparse_mla_decode_no_alloc(
     const void* q, const uint8_t* cache, int64_t num_slots, int32_t record_bytes, const int32_t* indices,
     int32_t batch, int32_t s_q, int32_t h_q, int32_t topk, float sm_scale, const float* attn_sink, void* out,
     float* lse, int32_t num_splits, uint32_t* dev_status, void* stream) {
+    int64_t rows = 0;
+    int sms = 0;
+    const int chk = nvfp4mla::check_decode_call(q, cache, num_slots, record_bytes, indices, batch, s_q, h_q, topk,
+                                                attn_sink, out, lse, num_splits, &rows, &sms);
+    if (chk != NVFP4_MLA_OK || rows == 0) return chk;
     size_t need = 0;
     const int st = nvfp4_sparse_mla_decode_workspace_size(batch, s_q, h_q, topk, record_bytes, num_splits, &need);
     if (st != NVFP4_MLA_OK) return st;
     if (need > kNoAllocScratchBytes) return NVFP4_MLA_ERR_WORKSPACE;
     void* scratch = nullptr;
     if (need > 0) {
-        const int s = scratch_address(&scratch);
+        const int s = scratch_address(static_cast<cudaStream_t>(stream), &scratch);
         if (s != NVFP4_MLA_OK) return s;
     }
     return nvfp4_sparse_mla_decode(q, cache, num_slots, record_bytes, indices, batch, s_q, h_q, topk, sm_scale,

@@ -33,6 +33,14 @@ struct DecodeArgs {
     uint32_t* dev_status;
 };
 
+// The host-side checks of a decode call, in the order the entry points apply them: shape and
+// record width, pointers and alignment (skipped when there are no rows), then a usable sm_103
+// device. Sets rows (batch x s_q) and sms (0 unless every check passed).
+int check_decode_call(const void* q, const uint8_t* cache, int64_t num_slots, int32_t record_bytes,
+                      const int32_t* indices, int32_t batch, int32_t s_q, int32_t h_q, int32_t topk,
+                      const float* attn_sink, const void* out, const float* lse, int32_t num_splits, int64_t* rows,
+                      int* sms);
+
 // Keys of one split, rounded to whole tiles.
 int decode_keys_per_split(int topk, int splits);
 cudaError_t launch_sparse_decode(const DecodeArgs& a, cudaStream_t stream);

@@ -134,12 +134,12 @@ def test_host_side_checks_return_codes_without_a_device(cdll):
         assert cdll.nvfp4_sparse_mla_decode_workspace_size(2, 1, 64, 64, bad, 2, ctypes.byref(n)) == lib.ERR_UNSUPPORTED
         assert cdll.nvfp4_mla_quantize_append(None, 512, None, 64, None, 4, None, 8, bad, None, None) == lib.ERR_UNSUPPORTED
     assert cdll.nvfp4_mla_quantize_append(None, 512, None, 64, None, 4, None, 8, 352 | blk, None, None) == lib.ERR_INVALID_ARG
-    # the no-allocation decode refuses a problem whose partials exceed its fixed scratch, and
-    # passes the shape checks through, before any CUDA call
+    # the no-allocation decode checks its arguments first, like the workspace entry point (its
+    # scratch limit, ERR_WORKSPACE, is checked on a GPU in test_zz_no_alloc.py)
     big = 64 * 64 * 128 * 512 * 2                 # 64 rows x 64 splits x 128 heads of f16 partials
     assert big > lib.NO_ALLOC_SCRATCH_BYTES
     assert cdll.nvfp4_sparse_mla_decode_no_alloc(None, None, 8, 352, None, 64, 1, 128, 4096, 1.0, None, None, None,
-                                                 64, None, None) == lib.ERR_WORKSPACE
+                                                 64, None, None) == lib.ERR_INVALID_ARG
     assert cdll.nvfp4_sparse_mla_decode_no_alloc(None, None, 8, 400, None, 1, 1, 128, 64, 1.0, None, None, None,
                                                  1, None, None) == lib.ERR_UNSUPPORTED
     # decode: null pointers

@@ -70,3 +70,28 @@ def test_no_alloc_rejects_problems_beyond_its_scratch_limit():
     lse = torch.zeros((5, 1, 128), dtype=torch.float32, device=DEV)
     st = _no_alloc(cdll, q, cache, idx, 0.1, None, out, lse, 64, None)
     assert st == lib.ERR_WORKSPACE
+
+
+@pytest.mark.parametrize("record_bytes,splits", [(352, 0), (432, 2), (352, 3)])
+def test_no_alloc_is_bit_identical_to_the_workspace_entry_point(record_bytes, splits):
+    """Both entry points run the same kernels with the same split count (num_splits = 0: the
+    library's own choice, which both must make alike), so out and lse agree bit for bit."""
+    cdll = lib.load(build_if_missing=True)
+    rng = np.random.default_rng(7 + record_bytes + splits)
+    B, s_q, h_q, topk, n_slots = 2, 1, 128, 900, 3000
+    cache = fill_pool(lib.quantize_append, n_slots, record_bytes, 5, DEV)
+    sink = torch.from_numpy(rng.standard_normal(h_q).astype(np.float32)).to(DEV)
+    q = torch.from_numpy(rng.standard_normal((B, s_q, h_q, 576)).astype(np.float32)).to(torch.bfloat16).to(DEV)
+    idx = np.stack([rng.choice(n_slots, topk, replace=False) for _ in range(B * s_q)]).astype(np.int32)
+    idx[rng.random(idx.shape) < 0.05] = -1
+    idx = torch.from_numpy(idx.reshape(B, s_q, topk)).to(DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = torch.full((B, s_q, h_q, 512), float("nan"), dtype=torch.bfloat16, device=DEV)
+    lse = torch.full((B, s_q, h_q), float("nan"), dtype=torch.float32, device=DEV)
+    st = _no_alloc(cdll, q, cache, idx, 1 / 24, sink, out, lse, splits, status)
+    assert st == lib.OK, lib.status_string(st)
+    ref_out, ref_lse = lib.sparse_mla_decode(q, cache, idx, 1 / 24, attn_sink=sink, num_splits=splits)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert torch.equal(out, ref_out)
+    assert torch.equal(lse, ref_lse)
