@@ -76,6 +76,8 @@ def lib() -> ctypes.CDLL:
             fn = getattr(_lib, name)
             fn.restype = None
             fn.argtypes = [intype, i64, outtype]
+        _lib.oracle_norm_rope.restype = None
+        _lib.oracle_norm_rope.argtypes = [P, i64, P, i64, P, i64, P, d, P, P, i64, i32, P, P, P, P, P, P]
         _lib.oracle_threads_available.restype = i32
         _lib.oracle_threads_available.argtypes = []
     return _lib
@@ -172,6 +174,30 @@ def quantize_append(latent_bits: np.ndarray, rope_bits: np.ndarray, slot_mapping
     return int(lib().oracle_quantize_append(
         _ptr(latent_bits), latent_bits.strides[0] // 2, _ptr(rope_bits), rope_bits.strides[0] // 2,
         _ptr(slots), T, _ptr(cache), cache.shape[0], record_bytes, _block_flag(record_bytes, block_scales)))
+
+
+def norm_rope(latent_bits: np.ndarray, rope_bits: np.ndarray, positions: np.ndarray, weight_bits: np.ndarray,
+              eps: float, cos_table: np.ndarray, sin_table: np.ndarray, rotate_half: bool) -> dict:
+    """The stage ahead of the append (RMSNorm of the latent, rotary embedding of k_pe), see
+    oracle_norm_rope. latent bf16 bits [T,512], k_pe [T,64] (strided rows allowed), positions
+    int64 [T], weight bf16 bits [512], cos/sin fp32 [num_positions, 32]. Returns a dict:
+    ``latent`` [T,512] and ``rope`` [T,64] bf16 bits, ``exact`` fp64 [T,576], ``flag`` and
+    ``other`` [T,576] (the other admissible bf16 rounding where flagged), ``valid`` [T]."""
+    assert latent_bits.dtype == np.uint16 and rope_bits.dtype == np.uint16
+    assert latent_bits.strides[1] == 2 and rope_bits.strides[1] == 2
+    pos = _c(positions, np.int64)
+    T = pos.size
+    w = _c(weight_bits, np.uint16)
+    cs, sn = _c(cos_table, np.float32), _c(sin_table, np.float32)
+    assert w.size == 512 and cs.shape == sn.shape and cs.shape[1] == 32
+    res = {"latent": np.zeros((T, 512), np.uint16), "rope": np.zeros((T, 64), np.uint16),
+           "exact": np.zeros((T, 576), np.float64), "flag": np.zeros((T, 576), np.uint8),
+           "other": np.zeros((T, 576), np.uint16), "valid": np.zeros(T, np.uint8)}
+    lib().oracle_norm_rope(_ptr(latent_bits), latent_bits.strides[0] // 2, _ptr(rope_bits), rope_bits.strides[0] // 2,
+                           _ptr(pos), T, _ptr(w), float(eps), _ptr(cs), _ptr(sn), cs.shape[0], int(bool(rotate_half)),
+                           _ptr(res["latent"]), _ptr(res["rope"]), _ptr(res["exact"]), _ptr(res["flag"]),
+                           _ptr(res["other"]), _ptr(res["valid"]))
+    return res
 
 
 def dequant_records(records: np.ndarray, block_scales: bool = False) -> np.ndarray:

@@ -379,6 +379,107 @@ void oracle_merge_partials(int P, const double* lse_p, const double* out_p, cons
 }
 
 /* Vector helpers so the Python side can check single-value conversions in bulk. */
+/* ---- the producer ahead of the append: RMSNorm + rotary embedding ------------------------
+ *
+ * [SGLang-38646] "[SM120] Add opt-in NVFP4 sparse-MLA KV cache format for DeepSeek-V4"
+ * (SGLang pull request 38646), "Limitations" (the NVFP4 path has no fused
+ * norm+rope+quantize+store kernel and pays a bf16 intermediate plus a separate quantize kernel)
+ * and "Stores" (the fused store kernels emit only the fp8 layout). The pages name the stages but
+ * fix none of their parameters; the readings used here:
+ *  - RMSNorm of the 512 latent values of a token: y_i = w_i * x_i / sqrt(mean_j x_j^2 + eps),
+ *    with a weight vector w (bf16) and eps given by the caller;
+ *  - rotary embedding of the 64 k_pe values at the token's position p, frequency f in 0..31
+ *    with c = cos_table[p][f], s = sin_table[p][f] (fp32 tables given by the caller), the pair
+ *    (a, b) of frequency f rotated to (a c - b s, b c + a s); pairs are (f, f + 32) ("rotate
+ *    half") or (2f, 2f + 1) ("interleaved"), a flag of the call;
+ *  - both in fp64 from the bf16 inputs, each result rounded once to bf16 (round to nearest,
+ *    ties to even): the same numbers the unfused path stores in its bf16 intermediate, which
+ *    the append then quantizes;
+ *  - a token whose position is outside [0, num_positions) is not written.
+ * A kernel computing in fp32 may round a value the other way when the exact value lies within
+ * its own error of a bf16 rounding midpoint. So every value whose exact result lies within
+ * 2^-16 times the size of its terms (|y_i| for the norm, |a c| + |b s| for the rotation) of a
+ * midpoint is flagged, with the other admissible bf16 value, and a test accepts either. */
+static const double kMidpointBand = 1.0 / 65536.0;
+
+/* bf16 bits of a double that is exactly a bf16 value */
+static uint16_t bf16_bits_of(double r) {
+    float f = (float)r;
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    return (uint16_t)(u >> 16);
+}
+
+/* Rounds v to bf16 (bits into *near); when v lies within `band` of the midpoint between the two
+ * bf16 values around it, *flag = 1 and *other = the bits of the other one; else *other = *near. */
+static void round_with_flag(double v, double band, uint16_t* near, uint16_t* other, uint8_t* flag) {
+    const double r = oracle_round_to_bf16(v);
+    *near = bf16_bits_of(r);
+    *other = *near;
+    *flag = 0;
+    if (v == r || !isfinite(r)) return;
+    /* the neighbour of r on v's side, one bf16 step away */
+    uint16_t nb = *near;
+    const int up = (v > r);            /* v lies above r */
+    const int neg = (nb & 0x8000) != 0;
+    if (r == 0.0) nb = (uint16_t)(up ? 0x0001 : 0x8001);
+    else nb = (uint16_t)((up != neg) ? nb + 1 : nb - 1);
+    const double n2 = oracle_bf16_to_double(nb);
+    const double mid = 0.5 * (r + n2);
+    if (fabs(v - mid) <= band) {
+        *flag = 1;
+        *other = nb;
+    }
+}
+
+/* latent [T, 512] and k_pe [T, 64] bf16 bits (row strides in elements), positions [T],
+ * weight [512] bf16 bits, cos/sin [num_positions, 32]. Outputs, per token: the normalized
+ * latent and rotated k_pe as bf16 bits (lat_out [T, 512], rope_out [T, 64]), the exact values
+ * (exact [T, 576], may be NULL), the flags and other admissible roundings (flag, other
+ * [T, 576], the latent first), and valid[T] (0: position out of range, nothing else set). */
+void oracle_norm_rope(const uint16_t* latent, int64_t latent_row_stride, const uint16_t* k_pe,
+                      int64_t rope_row_stride, const int64_t* positions, int64_t T,
+                      const uint16_t* weight, double eps, const float* cos_table, const float* sin_table,
+                      int64_t num_positions, int rotate_half, uint16_t* lat_out, uint16_t* rope_out,
+                      double* exact, uint8_t* flag, uint16_t* other, uint8_t* valid) {
+    for (int64_t t = 0; t < T; ++t) {
+        const int64_t p = positions[t];
+        valid[t] = (uint8_t)(p >= 0 && p < num_positions);
+        if (!valid[t]) continue;
+        const uint16_t* x = latent + t * latent_row_stride;
+        const uint16_t* k = k_pe + t * rope_row_stride;
+        /* RMSNorm */
+        double ss = 0.0;
+        for (int i = 0; i < 512; ++i) {
+            const double v = oracle_bf16_to_double(x[i]);
+            ss += v * v;
+        }
+        const double inv = 1.0 / sqrt(ss / 512.0 + eps);
+        for (int i = 0; i < 512; ++i) {
+            const double y = oracle_bf16_to_double(weight[i]) * oracle_bf16_to_double(x[i]) * inv;
+            if (exact) exact[t * 576 + i] = y;
+            round_with_flag(y, kMidpointBand * fabs(y), &lat_out[t * 512 + i], &other[t * 576 + i],
+                            &flag[t * 576 + i]);
+        }
+        /* rotary embedding */
+        for (int f = 0; f < 32; ++f) {
+            const int ia = rotate_half ? f : 2 * f;
+            const int ib = rotate_half ? f + 32 : 2 * f + 1;
+            const double a = oracle_bf16_to_double(k[ia]), b = oracle_bf16_to_double(k[ib]);
+            const double c = (double)cos_table[p * 32 + f], s = (double)sin_table[p * 32 + f];
+            const double oa = a * c - b * s, ob = b * c + a * s;
+            const double band = kMidpointBand * (fabs(a * c) + fabs(b * s));
+            const double bandb = kMidpointBand * (fabs(b * c) + fabs(a * s));
+            if (exact) {
+                exact[t * 576 + 512 + ia] = oa;
+                exact[t * 576 + 512 + ib] = ob;
+            }
+            round_with_flag(oa, band, &rope_out[t * 64 + ia], &other[t * 576 + 512 + ia], &flag[t * 576 + 512 + ia]);
+            round_with_flag(ob, bandb, &rope_out[t * 64 + ib], &other[t * 576 + 512 + ib], &flag[t * 576 + 512 + ib]);
+        }
+    }
+}
+
 void oracle_e4m3_encode_many(const float* f, int64_t n, uint8_t* out) {
     for (int64_t i = 0; i < n; ++i) out[i] = oracle_e4m3_encode(f[i]);
 }
