@@ -85,6 +85,8 @@ typedef enum {
 #define NVFP4_MLA_DEV_INDEX_OUT_OF_RANGE 0x2u /* decode: index >= num_slots (masked)          */
 #define NVFP4_MLA_DEV_TIMEOUT 0x4u            /* decode: a pipeline wait gave up; out invalid */
 #define NVFP4_MLA_DEV_FP8_RANGE 0x8u          /* quantize_append, 656 B: a NoPE |x| >= 65536  */
+#define NVFP4_MLA_DEV_POSITION_OUT_OF_RANGE 0x10u /* norm_rope_quantize_append: position outside
+                                                     [0, num_positions) (token skipped)         */
 
 /*
  * Quantize-and-append (write side).
@@ -107,6 +109,40 @@ NVFP4_MLA_API int nvfp4_mla_quantize_append(const void* kv_latent, int64_t laten
                                             const int64_t* slot_mapping, int64_t num_tokens,
                                             uint8_t* cache, int64_t num_slots, int32_t record_bytes,
                                             uint32_t* dev_status, void* stream);
+
+/*
+ * Fused producer: RMSNorm of the latent, rotary embedding of k_pe, quantize and append, in one
+ * kernel. SGLang PR 38646 "[SM120] Add opt-in NVFP4 sparse-MLA KV cache format for
+ * DeepSeek-V4", "Limitations": the NVFP4 path lacks the fused norm+rope+quantize+store kernel and
+ * pays a bf16 intermediate plus a separate quantize kernel per layer; "Stores": the existing
+ * fused store kernels emit only the fp8 layout. The pages fix none of the stages' parameters, so
+ * they are arguments here:
+ *   kv_latent          bf16 [num_tokens, 512] BEFORE the norm (layout as in quantize_append).
+ *   norm_weight        bf16 [512], 16-byte aligned: y_i = norm_weight[i] * x_i /
+ *                      sqrt(mean_j x_j^2 + eps).
+ *   eps                the norm's epsilon (>= 0).
+ *   k_pe               bf16 [num_tokens, 64] BEFORE the rotary embedding (layout as k_rope).
+ *   positions          int64 [num_tokens], 8-byte aligned: each token's position p. A position
+ *                      outside [0, num_positions) skips the token and sets
+ *                      NVFP4_MLA_DEV_POSITION_OUT_OF_RANGE.
+ *   cos_table,         fp32 [num_positions, 32] each, 8-byte aligned: cos and sin of frequency f
+ *   sin_table          at position p. The pair (a, b) of frequency f becomes (a c - b s, b c + a s).
+ *   rotate_half        1: the pair of frequency f is (k_pe[f], k_pe[f + 32]); 0: (k_pe[2f],
+ *                      k_pe[2f + 1]) ("interleaved").
+ *   slot_mapping, cache, num_slots, record_bytes, dev_status: as in quantize_append.
+ * Both stages compute in fp32 and round each result once to bf16, the value an unfused path
+ * stores in its bf16 intermediate; the records are then those quantize_append writes for these
+ * bf16 values. A result within about 2^-19 (relative to its terms) of a bf16 rounding midpoint may
+ * round to either neighbour. num_tokens == 0 is valid and launches nothing.
+ */
+NVFP4_MLA_API int nvfp4_mla_norm_rope_quantize_append(const void* kv_latent, int64_t latent_row_stride,
+                                                      const void* norm_weight, float eps, const void* k_pe,
+                                                      int64_t rope_row_stride, const int64_t* positions,
+                                                      const float* cos_table, const float* sin_table,
+                                                      int64_t num_positions, int32_t rotate_half,
+                                                      const int64_t* slot_mapping, int64_t num_tokens,
+                                                      uint8_t* cache, int64_t num_slots, int32_t record_bytes,
+                                                      uint32_t* dev_status, void* stream);
 
 /*
  * Scratch size of nvfp4_sparse_mla_decode for a problem (host-only, no CUDA call).

@@ -32,9 +32,11 @@ DEV_SLOT_OUT_OF_RANGE = 0x1
 DEV_INDEX_OUT_OF_RANGE = 0x2
 DEV_TIMEOUT = 0x4
 DEV_FP8_RANGE = 0x8
+DEV_POSITION_OUT_OF_RANGE = 0x10
 
 EXPORTED = (
     "nvfp4_mla_quantize_append",
+    "nvfp4_mla_norm_rope_quantize_append",
     "nvfp4_sparse_mla_decode_workspace_size",
     "nvfp4_sparse_mla_decode",
     "nvfp4_sparse_mla_decode_no_alloc",
@@ -70,6 +72,9 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
     P, i64, i32, f32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_float, ctypes.c_size_t
     lib.nvfp4_mla_quantize_append.restype = ctypes.c_int
     lib.nvfp4_mla_quantize_append.argtypes = [P, i64, P, i64, P, i64, P, i64, i32, P, P]
+    lib.nvfp4_mla_norm_rope_quantize_append.restype = ctypes.c_int
+    lib.nvfp4_mla_norm_rope_quantize_append.argtypes = [P, i64, P, f32, P, i64, P, P, P, i64, i32, P, i64, P, i64, i32,
+                                                        P, P]
     lib.nvfp4_sparse_mla_decode_workspace_size.restype = ctypes.c_int
     lib.nvfp4_sparse_mla_decode_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32, ctypes.POINTER(sz)]
     lib.nvfp4_sparse_mla_decode.restype = ctypes.c_int
@@ -136,6 +141,39 @@ def quantize_append(kv_latent: torch.Tensor, k_rope: torch.Tensor, slot_mapping:
         _ptr(kv_latent), kv_latent.stride(0), _ptr(k_rope), k_rope.stride(0), _ptr(slot_mapping), T,
         _ptr(cache), cache.shape[0], code, _ptr(dev_status), _stream(stream))
     _check("nvfp4_mla_quantize_append", st)
+
+
+def norm_rope_quantize_append(kv_latent: torch.Tensor, norm_weight: torch.Tensor, eps: float, k_pe: torch.Tensor,
+                              positions: torch.Tensor, cos_table: torch.Tensor, sin_table: torch.Tensor,
+                              rotate_half: bool, slot_mapping: torch.Tensor, cache: torch.Tensor,
+                              dev_status: Optional[torch.Tensor] = None, stream=None,
+                              block_scales: bool = False) -> None:
+    """RMSNorm ``kv_latent`` (bf16 [T,512], pre-norm) with ``norm_weight`` (bf16 [512]) and
+    ``eps``, rotate ``k_pe`` (bf16 [T,64], pre-rotation) by ``positions`` (int64 [T]) with
+    ``cos_table`` / ``sin_table`` (fp32 [P,32]), pairs (f, f+32) when ``rotate_half`` else
+    (2f, 2f+1); then quantize and write the records as quantize_append does, in one kernel."""
+    _need(kv_latent.dtype == torch.bfloat16 and k_pe.dtype == torch.bfloat16, "inputs must be bf16")
+    _need(kv_latent.dim() == 2 and kv_latent.shape[1] == D_NOPE and kv_latent.stride(1) == 1, "kv_latent [T,512], inner stride 1")
+    _need(k_pe.dim() == 2 and k_pe.shape[1] == D_ROPE and k_pe.stride(1) == 1, "k_pe [T,64], inner stride 1")
+    T = kv_latent.shape[0]
+    _need(k_pe.shape[0] == T and slot_mapping.numel() == T and positions.numel() == T, "token counts differ")
+    _need(norm_weight.dtype == torch.bfloat16 and norm_weight.numel() == D_NOPE and norm_weight.is_contiguous(),
+          "norm_weight bf16 [512] contiguous")
+    _need(positions.dtype == torch.int64 and positions.is_contiguous(), "positions int64 contiguous")
+    _need(cos_table.dtype == torch.float32 and sin_table.dtype == torch.float32 and cos_table.dim() == 2
+          and cos_table.shape[1] == 32 and cos_table.shape == sin_table.shape and cos_table.is_contiguous()
+          and sin_table.is_contiguous(), "cos_table / sin_table fp32 [P,32] contiguous")
+    _need(slot_mapping.dtype == torch.int64 and slot_mapping.is_contiguous(), "slot_mapping int64 contiguous")
+    _need(cache.dtype == torch.uint8 and cache.dim() == 2 and cache.is_contiguous(), "cache uint8 [num_slots, R] contiguous")
+    _need(cache.shape[1] in RECORD_BYTES, "record width must be 352, 432 or 656")
+    code = _record_code(cache, block_scales)
+    for t in (kv_latent, norm_weight, k_pe, positions, cos_table, sin_table, slot_mapping, cache):
+        _need(t.is_cuda and t.device == cache.device, "all tensors on the same CUDA device")
+    st = load().nvfp4_mla_norm_rope_quantize_append(
+        _ptr(kv_latent), kv_latent.stride(0), _ptr(norm_weight), ctypes.c_float(eps), _ptr(k_pe), k_pe.stride(0),
+        _ptr(positions), _ptr(cos_table), _ptr(sin_table), cos_table.shape[0], int(bool(rotate_half)),
+        _ptr(slot_mapping), T, _ptr(cache), cache.shape[0], code, _ptr(dev_status), _stream(stream))
+    _check("nvfp4_mla_norm_rope_quantize_append", st)
 
 
 def workspace_size(batch: int, s_q: int, h_q: int, topk: int, record_bytes: int, num_splits: int = 0) -> int:

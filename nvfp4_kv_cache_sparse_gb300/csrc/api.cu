@@ -137,6 +137,43 @@ NVFP4_MLA_API int nvfp4_mla_quantize_append(const void* kv_latent, int64_t laten
     return e == cudaSuccess ? NVFP4_MLA_OK : NVFP4_MLA_ERR_CUDA;
 }
 
+NVFP4_MLA_API int nvfp4_mla_norm_rope_quantize_append(const void* kv_latent, int64_t latent_row_stride,
+                                                      const void* norm_weight, float eps, const void* k_pe,
+                                                      int64_t rope_row_stride, const int64_t* positions,
+                                                      const float* cos_table, const float* sin_table,
+                                                      int64_t num_positions, int32_t rotate_half,
+                                                      const int64_t* slot_mapping, int64_t num_tokens,
+                                                      uint8_t* cache, int64_t num_slots, int32_t record_bytes,
+                                                      uint32_t* dev_status, void* stream) {
+    if (!record_ok(record_bytes)) return NVFP4_MLA_ERR_UNSUPPORTED;
+    if (num_tokens < 0 || num_slots < 0 || num_positions < 0 || !(eps >= 0.0f) || (rotate_half != 0 && rotate_half != 1))
+        return NVFP4_MLA_ERR_INVALID_ARG;
+    if (num_tokens == 0) return NVFP4_MLA_OK;
+    if (!kv_latent || !k_pe || !slot_mapping || !cache || !norm_weight || !positions || !cos_table || !sin_table)
+        return NVFP4_MLA_ERR_INVALID_ARG;
+    if (!aligned(kv_latent, 16) || !aligned(k_pe, 16) || !aligned(cache, 16) || !aligned(slot_mapping, 8) ||
+        !aligned(norm_weight, 16) || !aligned(positions, 8) || !aligned(cos_table, 8) || !aligned(sin_table, 8))
+        return NVFP4_MLA_ERR_INVALID_ARG;
+    if (latent_row_stride < 512 || latent_row_stride % 8 != 0) return NVFP4_MLA_ERR_INVALID_ARG;
+    if (rope_row_stride < 64 || rope_row_stride % 8 != 0) return NVFP4_MLA_ERR_INVALID_ARG;
+    int status = NVFP4_MLA_OK;
+    const int sms = device_sm_count(&status);
+    if (sms <= 0) return status;
+    nvfp4mla::ProducerArgs pr;
+    pr.norm_weight = static_cast<const uint16_t*>(norm_weight);
+    pr.eps = eps;
+    pr.positions = positions;
+    pr.cos_table = cos_table;
+    pr.sin_table = sin_table;
+    pr.num_positions = num_positions;
+    pr.rotate_half = rotate_half;
+    const cudaError_t e = nvfp4mla::launch_quantize_append(kv_latent, latent_row_stride, k_pe, rope_row_stride,
+                                                           slot_mapping, num_tokens, cache, num_slots,
+                                                           record_width(record_bytes), block_scales(record_bytes),
+                                                           dev_status, sms, static_cast<cudaStream_t>(stream), &pr);
+    return e == cudaSuccess ? NVFP4_MLA_OK : NVFP4_MLA_ERR_CUDA;
+}
+
 NVFP4_MLA_API int nvfp4_sparse_mla_decode_workspace_size(int32_t batch, int32_t s_q, int32_t h_q, int32_t topk,
                                                          int32_t record_bytes, int32_t num_splits, size_t* bytes) {
     if (!bytes) return NVFP4_MLA_ERR_INVALID_ARG;

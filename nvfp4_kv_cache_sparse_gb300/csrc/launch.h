@@ -8,10 +8,22 @@
 
 namespace nvfp4mla {
 
+// The fused producer stage ahead of the quantizer (nvfp4_mla_norm_rope_quantize_append).
+struct ProducerArgs {
+    const uint16_t* norm_weight;   // bf16 [512]
+    float eps;
+    const int64_t* positions;      // [num_tokens]
+    const float* cos_table;        // fp32 [num_positions, 32]
+    const float* sin_table;
+    int64_t num_positions;
+    int rotate_half;               // 1: pairs (f, f + 32); 0: pairs (2f, 2f + 1)
+};
+
 cudaError_t launch_quantize_append(const void* kv_latent, int64_t latent_row_stride, const void* k_rope,
                                    int64_t rope_row_stride, const int64_t* slot_mapping, int64_t num_tokens,
                                    uint8_t* cache, int64_t num_slots, int record_bytes, bool block_scales,
-                                   uint32_t* dev_status, int sm_count, cudaStream_t stream);
+                                   uint32_t* dev_status, int sm_count, cudaStream_t stream,
+                                   const ProducerArgs* producer = nullptr);
 
 struct DecodeArgs {
     const void* q;             // bf16 [rows, h_q, 576]

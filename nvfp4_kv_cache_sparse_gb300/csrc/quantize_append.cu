@@ -40,6 +40,18 @@
 // to T in fp32; otherwise amax / 6 lies at least 2^-10.6 (relative) from every tie point, far
 // beyond the product's error. Either way the e4m3 rounding equals that of amax / 6. Per block,
 // rn(1/s) of every e4m3 scale is kept in a shared table.
+//
+// Fused producer (kFused): SGLang PR 38646 "[SM120] Add opt-in NVFP4 sparse-MLA KV cache format
+// for DeepSeek-V4", "Limitations" (no fused norm+rope+quantize+store kernel for NVFP4, so the
+// path pays a bf16 intermediate and a separate quantize kernel) and "Stores". Ahead of the
+// quantizer, the kernel takes the pre-norm latent and the pre-rotation k_pe and computes, in
+// fp32, the RMSNorm y_i = w_i x_i / sqrt(mean_j x_j^2 + eps) (sum of squares by a warp butterfly,
+// so every lane holds the same sum) and the rotation of each k_pe pair (a, b) by the token's
+// position, (a c - b s, b c + a s), pairs (f, f + 32) or (2f, 2f + 1); each result is rounded
+// once to bf16, the value the unfused path would store in its intermediate, and then quantized
+// exactly as in the plain append. The fp32 results lie within about 2^-19 (relative to the
+// terms) of the exact ones, so the bf16 rounding can differ from the exact one only for values
+// that close to a rounding midpoint.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -53,6 +65,7 @@ namespace {
 constexpr int kWarpsPerBlock = 8;
 constexpr int kTokensPerRound = 2;
 constexpr int kBlocksPerSm = 4;
+constexpr int kFusedBlocksPerSm = 2;   // the producer stage holds the norm weights and more per token
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
@@ -105,11 +118,17 @@ __device__ __forceinline__ uint32_t e4m3x2_signed(float hi, float lo) {
     return r;
 }
 
-template <int R, bool kBlk>
-__global__ void __launch_bounds__(kWarpsPerBlock * 32, kBlocksPerSm)
+__device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+template <int R, bool kBlk, bool kFused>
+__global__ void __launch_bounds__(kWarpsPerBlock * 32, kFused ? kFusedBlocksPerSm : kBlocksPerSm)
 quantize_append_kernel(const uint16_t* __restrict__ latent, int64_t latent_stride, const uint16_t* __restrict__ rope,
                        int64_t rope_stride, const int64_t* __restrict__ slot_mapping, int64_t num_tokens,
-                       uint8_t* __restrict__ cache, int64_t num_slots, uint32_t* __restrict__ dev_status) {
+                       uint8_t* __restrict__ cache, int64_t num_slots, uint32_t* __restrict__ dev_status,
+                       const ProducerArgs pr) {
     __shared__ __align__(16) uint8_t stage[kWarpsPerBlock][R];
     __shared__ float inv_scale[128];   // rn(1 / value) of each e4m3 scale code; 0 for code 0
     // A decode launched next on the stream may start its prologue now; it waits for this grid
@@ -124,6 +143,18 @@ quantize_append_kernel(const uint16_t* __restrict__ latent, int64_t latent_strid
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     uint8_t* rec = stage[warp];
+    // fused producer: the lane's 16 norm weights (group `lane`), and its rotation frequencies
+    uint32_t nw[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+    int freq = 0;
+    if constexpr (kFused) {
+        const uint4 a = __ldg(reinterpret_cast<const uint4*>(pr.norm_weight) + 2 * lane);
+        const uint4 b = __ldg(reinterpret_cast<const uint4*>(pr.norm_weight) + 2 * lane + 1);
+        nw[0] = a.x; nw[1] = a.y; nw[2] = a.z; nw[3] = a.w;
+        nw[4] = b.x; nw[5] = b.y; nw[6] = b.z; nw[7] = b.w;
+        // rotate half: elements 2 lane, 2 lane + 1 have frequencies (2 lane) % 32 and the next;
+        // interleaved: the lane's two elements are the pair of frequency `lane`
+        freq = pr.rotate_half ? (2 * lane) & 31 : lane;
+    }
 
     // kTokensPerRound tokens per warp per round. The loads of a round (slot, 32 latent bytes and
     // 4 RoPE bytes per lane per token) are issued before the previous round is converted, so a
@@ -133,6 +164,7 @@ quantize_append_kernel(const uint16_t* __restrict__ latent, int64_t latent_strid
         int64_t slot[kTokensPerRound];
         uint4 va[kTokensPerRound], vb[kTokensPerRound];
         uint32_t rw[kTokensPerRound];
+        int64_t pos[kTokensPerRound];   // fused producer only
     };
     auto load_round = [&](int64_t t0, Round& r) {
 #pragma unroll
@@ -145,6 +177,7 @@ quantize_append_kernel(const uint16_t* __restrict__ latent, int64_t latent_strid
                 r.va[u] = __ldg(src);
                 r.vb[u] = __ldg(src + 1);
                 r.rw[u] = __ldg(reinterpret_cast<const uint32_t*>(rope + t * rope_stride) + lane);
+                if constexpr (kFused) r.pos[u] = __ldg(pr.positions + t);
             }
         }
     };
@@ -166,7 +199,48 @@ quantize_append_kernel(const uint16_t* __restrict__ latent, int64_t latent_strid
                 continue;
             }
             // ---- NoPE group `lane`: 16 bf16 values
-            const uint32_t w[8] = {va[u].x, va[u].y, va[u].z, va[u].w, vb[u].x, vb[u].y, vb[u].z, vb[u].w};
+            uint32_t w[8] = {va[u].x, va[u].y, va[u].z, va[u].w, vb[u].x, vb[u].y, vb[u].z, vb[u].w};
+            uint32_t rwv = rw[u];
+            if constexpr (kFused) {
+                const int64_t p = cur.pos[u];
+                if (p < 0 || p >= pr.num_positions) {
+                    if (lane == 0 && dev_status != nullptr) atomicOr(dev_status, 0x10u);
+                    continue;
+                }
+                // the rotation's cos / sin first: their loads overlap the norm
+                float c0, c1, s0, s1;
+                if (pr.rotate_half) {
+                    const float2 c = __ldg(reinterpret_cast<const float2*>(pr.cos_table + p * 32 + freq));
+                    const float2 sn = __ldg(reinterpret_cast<const float2*>(pr.sin_table + p * 32 + freq));
+                    c0 = c.x; c1 = c.y; s0 = sn.x; s1 = sn.y;
+                } else {
+                    c0 = c1 = __ldg(pr.cos_table + p * 32 + freq);
+                    s0 = s1 = __ldg(pr.sin_table + p * 32 + freq);
+                }
+                // RMSNorm of the token's 512 values
+                float ss = 0.0f;
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    ss = fmaf(bf16_lo(w[k]), bf16_lo(w[k]), ss);
+                    ss = fmaf(bf16_hi(w[k]), bf16_hi(w[k]), ss);
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);   // same sum in every lane
+                const float inv = __fdiv_rn(1.0f, __fsqrt_rn(fmaf(ss, 1.0f / 512.0f, pr.eps)));
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    w[k] = bf16x2_rn(bf16_lo(w[k]) * bf16_lo(nw[k]) * inv, bf16_hi(w[k]) * bf16_hi(nw[k]) * inv);
+                // rotation of the lane's two k_pe values
+                const float e0 = bf16_lo(rwv), e1 = bf16_hi(rwv);
+                if (pr.rotate_half) {
+                    // partner elements +-32 live in lane ^ 16; the first half subtracts b s
+                    const uint32_t pw = __shfl_xor_sync(0xffffffffu, rwv, 16);
+                    const float sg = lane < 16 ? -1.0f : 1.0f;
+                    rwv = bf16x2_rn(fmaf(e0, c0, sg * (bf16_lo(pw) * s0)), fmaf(e1, c1, sg * (bf16_hi(pw) * s1)));
+                } else {
+                    rwv = bf16x2_rn(fmaf(e0, c0, -(e1 * s0)), fmaf(e1, c0, e0 * s0));
+                }
+            }
             // group maximum on |bf16| bit patterns (non-negative floats order like integers), two
             // per 32-bit word
             uint32_t m2 = max_u16x2(max_u16x2(max_u16x2(w[0] & 0x7FFF7FFFu, w[1] & 0x7FFF7FFFu),
@@ -193,7 +267,7 @@ quantize_append_kernel(const uint16_t* __restrict__ latent, int64_t latent_strid
                 }
                 *reinterpret_cast<uint4*>(rec + 16 * lane) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
                 if ((lane & 7) == 0) *reinterpret_cast<float*>(rec + 512 + 4 * (lane >> 3)) = scale;
-                *reinterpret_cast<uint32_t*>(rec + 528 + 4 * lane) = rw[u];
+                *reinterpret_cast<uint32_t*>(rec + 528 + 4 * lane) = rwv;
             } else {
             const float amax = __uint_as_float(amax_bits << 16);
             const uint32_t sbyte = e4m3x2_rn_sat(0.0f, amax * (1.0f / 6.0f)) & 0xFFu;
@@ -215,11 +289,11 @@ quantize_append_kernel(const uint16_t* __restrict__ latent, int64_t latent_strid
             // ---- RoPE: lane owns elements 2*lane and 2*lane+1
             if constexpr (R == 352) {
                 rec[kBlk ? 320 + lane : 320 + 8 * (lane & 3) + (lane >> 2)] = static_cast<uint8_t>(sbyte);
-                const uint32_t c = e4m3x2_signed(bf16_hi(rw[u]), bf16_lo(rw[u]));
+                const uint32_t c = e4m3x2_signed(bf16_hi(rwv), bf16_lo(rwv));
                 *reinterpret_cast<uint16_t*>(rec + 256 + 2 * lane) = static_cast<uint16_t>(c);
             } else {
                 rec[256 + lane] = static_cast<uint8_t>(sbyte);
-                *reinterpret_cast<uint32_t*>(rec + 304 + 4 * lane) = rw[u];
+                *reinterpret_cast<uint32_t*>(rec + 304 + 4 * lane) = rwv;
                 if (lane < 4) *reinterpret_cast<uint32_t*>(rec + 288 + 4 * lane) = 0u;
             }
             }
@@ -239,9 +313,10 @@ quantize_append_kernel(const uint16_t* __restrict__ latent, int64_t latent_strid
 cudaError_t launch_quantize_append(const void* kv_latent, int64_t latent_row_stride, const void* k_rope,
                                    int64_t rope_row_stride, const int64_t* slot_mapping, int64_t num_tokens,
                                    uint8_t* cache, int64_t num_slots, int record_bytes, bool block_scales,
-                                   uint32_t* dev_status, int sm_count, cudaStream_t stream) {
+                                   uint32_t* dev_status, int sm_count, cudaStream_t stream,
+                                   const ProducerArgs* producer) {
     const int64_t want = (num_tokens + kWarpsPerBlock - 1) / kWarpsPerBlock;
-    const int64_t cap = static_cast<int64_t>(sm_count) * kBlocksPerSm;   // one wave of resident blocks
+    const int64_t cap = static_cast<int64_t>(sm_count) * (producer ? kFusedBlocksPerSm : kBlocksPerSm);   // one wave
     const int grid = static_cast<int>(want < cap ? want : cap);
     const dim3 block(kWarpsPerBlock * 32);
     const auto* lat = static_cast<const uint16_t*>(kv_latent);
@@ -256,12 +331,14 @@ cudaError_t launch_quantize_append(const void* kv_latent, int64_t latent_row_str
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const auto kernel = record_bytes == 656 ? quantize_append_kernel<656, false>
-                        : record_bytes == 432 ? quantize_append_kernel<432, false>
-                        : block_scales      ? quantize_append_kernel<352, true>
-                                            : quantize_append_kernel<352, false>;
+    const bool f = producer != nullptr;
+    const auto kernel = record_bytes == 656 ? (f ? quantize_append_kernel<656, false, true> : quantize_append_kernel<656, false, false>)
+                        : record_bytes == 432 ? (f ? quantize_append_kernel<432, false, true> : quantize_append_kernel<432, false, false>)
+                        : block_scales ? (f ? quantize_append_kernel<352, true, true> : quantize_append_kernel<352, true, false>)
+                                       : (f ? quantize_append_kernel<352, false, true> : quantize_append_kernel<352, false, false>);
+    const ProducerArgs pr = f ? *producer : ProducerArgs{};
     const cudaError_t err = cudaLaunchKernelEx(&cfg, kernel, lat, latent_row_stride, rope, rope_row_stride,
-                                               slot_mapping, num_tokens, cache, num_slots, dev_status);
+                                               slot_mapping, num_tokens, cache, num_slots, dev_status, pr);
     return err != cudaSuccess ? err : cudaGetLastError();
 }
 

@@ -155,6 +155,38 @@ def write_path(seed: int = 0, T: int = 65_536, num_slots: int = 262_144,
                          bf16_from_f32(lat), bf16_from_f32(rope), torch.from_numpy(slots))
 
 
+@dataclass
+class ProducerWorkload:
+    """Inputs of the fused producer (norm + rotary embedding + quantize + append): the write
+    workload's latent and k_pe taken as the PRE-norm / PRE-rotation values, plus the stage
+    parameters a caller supplies."""
+    write: WriteWorkload
+    norm_weight: torch.Tensor       # bf16 [512]
+    eps: float
+    positions: torch.Tensor         # int64 [T]
+    cos_table: torch.Tensor         # fp32 [num_positions, 32]
+    sin_table: torch.Tensor         # fp32 [num_positions, 32]
+    rotate_half: bool
+
+
+def producer_inputs(seed: int = 0, T: int = 65_536, num_slots: int = 262_144, record_bytes: int = 352,
+                    num_positions: int = 65_536, rotate_half: bool = True,
+                    rope_base: float = 10_000.0) -> ProducerWorkload:
+    """write_path's tokens with per-token magnitudes spread over 2^-8 .. 2^8 (the norm removes
+    them), a norm weight ~ 1 + 0.1 N(0,1), eps 1e-6, positions uniform in [0, num_positions),
+    and the usual rotary tables: angle p * rope_base^(-f/32) for frequency f."""
+    w = write_path(seed=seed, T=T, num_slots=num_slots, record_bytes=record_bytes)
+    rng = np.random.default_rng(seed + 1)
+    mag = np.exp2(rng.uniform(-8, 8, (T, 1))).astype(np.float32)
+    lat = w.latent.float().numpy() * mag
+    w.latent = bf16_from_f32(lat)
+    weight = bf16_from_f32((1.0 + 0.1 * rng.standard_normal(D_NOPE)).astype(np.float32))
+    pos = rng.integers(0, num_positions, T).astype(np.int64)
+    ang = np.arange(num_positions, dtype=np.float64)[:, None] * (rope_base ** (-np.arange(32) / 32.0))[None, :]
+    return ProducerWorkload(w, weight, 1e-6, torch.from_numpy(pos), torch.from_numpy(np.cos(ang).astype(np.float32)),
+                            torch.from_numpy(np.sin(ang).astype(np.float32)), rotate_half)
+
+
 def _positions_to_slots(page_table: np.ndarray, pos: np.ndarray) -> np.ndarray:
     return page_table[pos // PAGE] * PAGE + pos % PAGE
 
