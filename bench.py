@@ -41,11 +41,11 @@ UNIT = "query-tokens/s"
 N_SETS = 8
 PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
-# DRAM bytes (read + write) of one sparse_decode_kernel launch on this workload, from an ncu
+# DRAM bytes (read + write) of one decode_pair_kernel launch on this workload, from an ncu
 # capture (dram__bytes_read.sum + dram__bytes_write.sum), keyed by the hash of the decode code
-# (comments removed) it was taken with; reported as null once that code changes. The merge kernel that follows it
-# re-reads the partials, which are L2-resident outside ncu's cache flushing.
-NCU_TRAFFIC = {"77755f3d8009": 34213376 + 29184}
+# (comments removed) it was taken with; reported as null once that code changes.
+NCU_TRAFFIC = {}
+DECODE_CALLS_TIMED = 128   # the decode call alone: 16 laps of 8 back-to-back calls
 
 
 def load_peaks():
@@ -71,8 +71,11 @@ def code_hash(text: str) -> str:
 
 
 def decode_source_hash() -> str:
-    src = os.path.join(ROOT, "nvfp4_kv_cache_sparse_gb300", "csrc", "sparse_decode.cu")
+    src = os.path.join(ROOT, "nvfp4_kv_cache_sparse_gb300", "csrc", "sparse_decode_pair.cu")
     return code_hash(open(src).read())
+
+
+
 
 
 # ---------------------------------------------------------------------------------------
@@ -265,7 +268,6 @@ def run_gpu(args):
     lse = torch.empty((w0.B, w0.s_q, w0.h_q), dtype=torch.float32, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream()
-    launches_per_step = 2 + (1 if ws_bytes > 0 else 0)
 
     def append(k, s):
         lat, rope, slots = news[k % N_SETS]
@@ -337,19 +339,24 @@ def run_gpu(args):
         end.record(stream)
         torch.cuda.synchronize()
         barrier(world)
-        # the decode call alone (kernel + merge): laps of N_SETS back-to-back calls, each lap
-        # between its own pair of events
-        n_laps = max(1, args.steps // N_SETS)
-        for k in range(n_laps):
-            evs[k][0].record(stream)
+        # the decode call alone: DECODE_CALLS_TIMED calls in laps of N_SETS back-to-back calls,
+        # each lap between its own pair of events, whatever --steps is
+        n_laps = DECODE_CALLS_TIMED // N_SETS
+        lap_evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_laps)]
+        for a, b in lap_evs:
+            a.record(stream)
             g_decode_lap.replay()
-            evs[k][1].record(stream)
+            b.record(stream)
         torch.cuda.synchronize()
     t_local = start.elapsed_time(end) / 1e3
     t_job = max_over_ranks(t_local, world, dev)
-    decode_ms = [a.elapsed_time(b) / N_SETS for a, b in evs[:n_laps]]
-    decode_s = statistics.mean(decode_ms) / 1e3
+    decode_us_laps = sorted(a.elapsed_time(b) / N_SETS * 1e3 for a, b in lap_evs)
+    decode_s = statistics.median(decode_us_laps) / 1e6
+    pct = lambda f: float(np.percentile(decode_us_laps, f))   # noqa: E731
     clocks = sampler.summary()
+    # kernels per call, as the library plans them for this shape on this device
+    _, decode_launches = lib.decode_plan(w0.B, w0.s_q, w0.h_q, w0.topk, w0.record_bytes, splits)
+    append_launches = 1
 
     # ---- end to end through the public API with host buffers: every step copies its inputs in
     # from pinned host memory and its result out. Device inputs and outputs are double-buffered
@@ -420,6 +427,10 @@ def run_gpu(args):
         peak = float(peaks["bf16_tflops"])
         traffic = NCU_TRAFFIC.get(decode_source_hash())
         cpu = cpu_baseline(args, w0) if (world == 1 and not args.no_cpu_baseline) else None
+        configs = None
+        if world == 1 and not args.no_configs:
+            configs = measure_configs(dev, args.config_iters)
+        launches = decode_launches + append_launches
         result = {
             "metric": METRIC,
             "value": job_throughput(w0.n_rows * args.steps, world, t_job),
@@ -451,10 +462,15 @@ def run_gpu(args):
                 "unit": "TFLOP/s",
                 "frac": achieved / peak,
                 "traffic": traffic,
-                "kernel": "decode call (sparse_decode_kernel + combine_kernel), CUDA events on the launch stream around "
-                          "laps of back-to-back calls over the same rotating inputs (graph-replayed)",
+                "kernel": "decode call (decode_pair_kernel, the splits merged inside it), CUDA events on the launch "
+                          f"stream around {n_laps} laps of {N_SETS} back-to-back calls over the rotating inputs "
+                          "(graph-replayed); median lap",
                 "peak_source": f"{peak_src} bf16 burst",
                 "decode_us": decode_s * 1e6,
+                "decode_us_p10": pct(10),
+                "decode_us_p90": pct(90),
+                "decode_calls_timed": n_laps * N_SETS,
+                "decode_kernels_per_call": decode_launches,
                 "roofline_us": max(flops / (peak * 1e12), alg_bytes / (float(peaks["hbm_gbs"]) * 1e9)) * 1e6,
                 "algorithmic_flops": flops,
                 "algorithmic_bytes": alg_bytes,
@@ -462,8 +478,9 @@ def run_gpu(args):
             "cpu_baseline": cpu,
             "e2e": {"value": job_throughput(w0.n_rows * args.steps, world, t_e2e), "unit": UNIT,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-            "gpu_launches": launches_per_step * args.steps,
+            "gpu_launches": launches * args.steps,
             "clocks": clocks,
+            "configs": configs,
         }
     barrier(world)
     return result
@@ -474,9 +491,10 @@ def run_gpu(args):
 # ---------------------------------------------------------------------------------------
 
 class OracleStep:
-    """The oracle's pass over sampled rows of one batch: append of their new tokens + decode."""
+    """The oracle's pass over sampled rows of one batch: append of their new tokens + decode
+    (threads: OpenMP threads of the decode, 0 = all host cores)."""
 
-    def __init__(self, w: synth.DecodeWorkload, rows: np.ndarray):
+    def __init__(self, w: synth.DecodeWorkload, rows: np.ndarray, threads: int = 0):
         import oracle
         self.oracle = oracle
         slots, q, idx = synth.compact_for_rows(w, rows)
@@ -491,10 +509,11 @@ class OracleStep:
         self.new_rope = synth.bf16_bits(nr)[: rows.size]
         self.new_slots = np.arange(slots.size, slots.size + rows.size, dtype=np.int64)
         self.rows = rows.size
+        self.threads = threads
 
     def __call__(self):
         self.oracle.quantize_append(self.new_lat, self.new_rope, self.new_slots, self.cache)
-        self.oracle.sparse_mla_decode(self.q, self.cache, self.idx, self.w.sm_scale)
+        self.oracle.sparse_mla_decode(self.q, self.cache, self.idx, self.w.sm_scale, threads=self.threads)
         return self.rows
 
 
@@ -539,10 +558,23 @@ def cpu_baseline(args, w):
         el = time.perf_counter() - t0
         if el >= args.cpu_seconds or reps >= 50:
             break
+    # the same oracle on one core: a bounded sample of rows (the whole step would take minutes)
+    one = OracleStep(w, rows[: args.cpu_rows_1core], threads=1)
+    t1 = time.perf_counter()
+    done1, reps1 = 0, 0
+    while True:
+        done1 += one()
+        reps1 += 1
+        el1 = time.perf_counter() - t1
+        if el1 >= args.cpu_seconds / 2 or reps1 >= 50:
+            break
     return {"value": done / el, "unit": UNIT, "cores": oracle.threads_available(), "kind": "oracle",
             "sample": f"{reps} x one full step ({w.n_rows} rows x {w.h_q} heads x {w.topk} keys, plus the "
                       f"{w.n_rows} appended tokens), fp64 C oracle, OpenMP over heads",
-            "seconds": el}
+            "seconds": el,
+            "single_core": {"value": done1 / el1, "unit": UNIT, "cores": 1,
+                            "sample": f"{reps1} x {one.rows} of the step's rows (all heads, all keys) plus their "
+                                      f"appended tokens, one OpenMP thread", "seconds": el1}}
 
 
 def run_reference(args):
@@ -614,58 +646,142 @@ def _time_calls(fn, iters: int, flush=None) -> float:
     return float(np.median(times))
 
 
-def run_sweep(args):
+DECODE_CONFIGS = (
+    ("tiny_b1_h64_topk64_R352", lambda: synth.tiny_decode(seed=0)),
+    ("varlen_b128_sq2_h64_topk2048_R352_sink", lambda: synth.varlen_decode(seed=0)),
+    ("longctx_b64_sq1_h128_topk2048_R432", lambda: synth.long_context(seed=0)),
+    ("prefill_b2_sq256_h128_topk2048_prefix16384_R352", lambda: synth.sparse_prefill(seed=0)),
+    # the batch decode over 656-byte fp8 records (the NVFP4-vs-fp8 comparison)
+    ("decode_b32_sq1_h128_topk2048_R656", lambda: dataclasses.replace(synth.batch_decode(seed=0), record_bytes=656)),
+)
+
+
+def measure_decode(w, dev, iters, flush, peaks):
     import nvfp4_kv_cache_sparse_gb300 as lib
     from synth.pool import fill_pool
+    tflops, hbm = float(peaks["bf16_tflops"]), float(peaks["hbm_gbs"])
+    cache = fill_pool(lib.quantize_append, w.num_slots, w.record_bytes, w.pool_seed, dev)
+    q, idx = w.q.to(dev), w.indices.to(dev)
+    sink = None if w.attn_sink is None else w.attn_sink.to(dev)
+    out = torch.empty((w.B, w.s_q, w.h_q, 512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((w.B, w.s_q, w.h_q), dtype=torch.float32, device=dev)
+    ws = torch.empty(max(1, lib.workspace_size(w.B, w.s_q, w.h_q, w.topk, w.record_bytes, 0)), dtype=torch.uint8,
+                     device=dev)
+
+    def call():
+        lib.sparse_mla_decode(q, cache, idx, w.sm_scale, attn_sink=sink, out=out, lse=lse, workspace=ws)
+
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(torch.cuda.current_device())
+    with sampler:
+        warm = _time_calls(call, iters)
+        cold = _time_calls(call, iters, flush)
+    flops, bytes_ = roofline_numbers(w)
+    t_roof = max(bytes_ / (hbm * 1e9), flops / (tflops * 1e12))
+    res = {"kind": "decode", "query_tokens": w.n_rows, "us_per_call_warm": warm * 1e6, "us_per_call_cold": cold * 1e6,
+           "query_tokens_per_s_cold": w.n_rows / cold, "roofline_us": t_roof * 1e6, "roofline_frac_cold": t_roof / cold,
+           "roofline_frac_warm": t_roof / warm,
+           "bound": "tensor" if flops / (tflops * 1e12) > bytes_ / (hbm * 1e9) else "hbm",
+           "algorithmic_flops": flops, "algorithmic_bytes": bytes_,
+           "valid_index_fraction": int((w.indices >= 0).sum()) / w.indices.numel(), "calls_timed": iters,
+           "clocks": sampler.summary()}
+    del cache
+    torch.cuda.empty_cache()
+    return res
+
+
+def measure_write(ww, dev, iters, flush, peaks, producer=None):
+    """The append (or, with a producer workload, the fused norm + rotary + append and the unfused
+    path it replaces: torch norm and rotation into a bf16 intermediate, then the append)."""
+    import nvfp4_kv_cache_sparse_gb300 as lib
+    hbm = float(peaks["hbm_gbs"])
+    cache = torch.full((ww.num_slots, ww.record_bytes), ww.fill_byte, dtype=torch.uint8, device=dev)
+    lat, rope, slots = ww.latent.to(dev), ww.rope.to(dev), ww.slot_mapping.to(dev)
+    if producer is None:
+        def call():
+            lib.quantize_append(lat, rope, slots, cache)
+        bytes_ = ww.T * (512 * 2 + 64 * 2 + 8 + ww.record_bytes)
+    else:
+        pw = producer
+        nw, pos = pw.norm_weight.to(dev), pw.positions.to(dev)
+        cos, sin = pw.cos_table.to(dev), pw.sin_table.to(dev)
+
+        def call():
+            lib.norm_rope_quantize_append(lat, nw, pw.eps, rope, pos, cos, sin, pw.rotate_half, slots, cache)
+
+        def unfused():
+            y = torch.nn.functional.rms_norm(lat.float(), (512,), weight=nw.float(), eps=pw.eps).to(torch.bfloat16)
+            c, s_ = cos[pos], sin[pos]
+            a, b = rope[:, :32].float(), rope[:, 32:].float()
+            r = torch.cat([a * c - b * s_, b * c + a * s_], dim=1).to(torch.bfloat16)
+            lib.quantize_append(y, r, slots, cache)
+        # + the position (8 B) and the token's cos / sin rows (256 B, from L2 for hot positions)
+        bytes_ = ww.T * (512 * 2 + 64 * 2 + 8 + 8 + ww.record_bytes)
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(torch.cuda.current_device())
+    with sampler:
+        warm = _time_calls(call, iters)
+        cold = _time_calls(call, iters, flush)
+        unf = _time_calls(unfused, max(5, iters // 4), flush) if producer is not None else None
+    t_roof = bytes_ / (hbm * 1e9)
+    res = {"kind": "quantize_append" if producer is None else "norm_rope_quantize_append", "tokens": ww.T,
+           "us_per_call_warm": warm * 1e6, "us_per_call_cold": cold * 1e6, "tokens_per_s_cold": ww.T / cold,
+           "achieved_gbs_cold": bytes_ / cold / 1e9, "roofline_us": t_roof * 1e6, "roofline_frac_cold": t_roof / cold,
+           "bound": "hbm", "algorithmic_bytes": bytes_, "calls_timed": iters, "clocks": sampler.summary()}
+    if unf is not None:
+        res["unfused_us_per_call_cold"] = unf * 1e6
+        res["unfused_path"] = "torch rms_norm and rotation into a bf16 intermediate, then quantize_append"
+    del cache
+    torch.cuda.empty_cache()
+    return res
+
+
+def measure_configs(dev, iters) -> dict:
+    """Every configuration besides the headline one, at N=1: cold and warm microseconds per call,
+    roofline fraction and the clocks seen while timing it (the default line carries them)."""
+    peaks, _ = load_peaks()
+    scrub = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+
+    def flush():
+        scrub.fill_(1)
+
+    res = {}
+    for name, make in DECODE_CONFIGS:
+        res[name] = measure_decode(make(), dev, iters, flush, peaks)
+    for R in (352, 656):
+        ww = synth.write_path(seed=0, record_bytes=R)
+        res[ww.name] = measure_write(ww, dev, iters, flush, peaks)
+    pw = synth.producer_inputs(seed=0, record_bytes=352)
+    res["norm_rope_" + pw.write.name] = measure_write(pw.write, dev, iters, flush, peaks, producer=pw)
+    del scrub
+    torch.cuda.empty_cache()
+    return res
+
+
+def run_sweep(args):
+    """Every configuration, one JSON line each (not the bench line), with the oracle's rate on a
+    sample of each."""
     dev = torch.device("cuda", 0)
     peaks, peak_src = load_peaks()
-    tflops, hbm = float(peaks["bf16_tflops"]), float(peaks["hbm_gbs"])
     scrub = torch.empty(512 << 20, dtype=torch.uint8, device=dev)   # > L2: written before cold calls
 
     def flush():
         scrub.fill_(1)
 
     iters = max(5, args.sweep_iters)
-    decode_cfgs = [("tiny_b1_h64_topk64_R352", synth.tiny_decode(seed=0)),
-                   ("decode_b32_sq1_h128_topk2048_R352", synth.batch_decode(seed=0)),
-                   ("varlen_b128_sq2_h64_topk2048_R352_sink", synth.varlen_decode(seed=0)),
-                   ("longctx_b64_sq1_h128_topk2048_R432", synth.long_context(seed=0)),
-                   ("prefill_b2_sq256_h128_topk2048_prefix16384_R352", synth.sparse_prefill(seed=0)),
-                   # the same batch decode over 656-byte fp8 records (the NVFP4-vs-fp8 comparison)
-                   ("decode_b32_sq1_h128_topk2048_R656",
-                    dataclasses.replace(synth.batch_decode(seed=0), record_bytes=656))]
+    cfgs = (("decode_b32_sq1_h128_topk2048_R352", lambda: synth.batch_decode(seed=0)),) + DECODE_CONFIGS
     want = lambda name: args.sweep_filter is None or args.sweep_filter in name   # noqa: E731
-    for name, w in decode_cfgs:
+    for name, make in cfgs:
         if not want(name):
             continue
-        cache = fill_pool(lib.quantize_append, w.num_slots, w.record_bytes, w.pool_seed, dev)
-        q, idx = w.q.to(dev), w.indices.to(dev)
-        sink = None if w.attn_sink is None else w.attn_sink.to(dev)
-        out = torch.empty((w.B, w.s_q, w.h_q, 512), dtype=torch.bfloat16, device=dev)
-        lse = torch.empty((w.B, w.s_q, w.h_q), dtype=torch.float32, device=dev)
-        ws = torch.empty(max(1, lib.workspace_size(w.B, w.s_q, w.h_q, w.topk, w.record_bytes, 0)), dtype=torch.uint8,
-                         device=dev)
-
-        def call():
-            lib.sparse_mla_decode(q, cache, idx, w.sm_scale, attn_sink=sink, out=out, lse=lse, workspace=ws)
-
-        for _ in range(3):
-            call()
-        torch.cuda.synchronize()
-        warm = _time_calls(call, iters)
-        cold = _time_calls(call, iters, flush)
-        flops, bytes_ = roofline_numbers(w)
-        t_roof = max(bytes_ / (hbm * 1e9), flops / (tflops * 1e12))
-        valid = int((w.indices >= 0).sum())
-        print(json.dumps({"sweep": True, "workload": name, "kind": "decode", "query_tokens": w.n_rows,
-                          "us_per_call_warm": warm * 1e6, "us_per_call_cold": cold * 1e6,
-                          "query_tokens_per_s_cold": w.n_rows / cold, "roofline_us": t_roof * 1e6,
-                          "roofline_frac_cold": t_roof / cold, "bound": "tensor" if flops / (tflops * 1e12) >
-                          bytes_ / (hbm * 1e9) else "hbm", "algorithmic_flops": flops, "algorithmic_bytes": bytes_,
-                          "valid_index_fraction": valid / w.indices.numel(), "peaks": peak_src,
-                          **oracle_decode_rate(w)}), flush=True)
-        del cache
-        torch.cuda.empty_cache()
+        w = make()
+        line = {"sweep": True, "workload": name, **measure_decode(w, dev, iters, flush, peaks), "peaks": peak_src,
+                **oracle_decode_rate(w)}
+        print(json.dumps(line), flush=True)
     # scale-layout comparison (FlashMLA PR 18, format block: the permuted scale placement is
     # credited with 10-12% of decode latency): the batch decode workload on two pools of the same
     # contents, one with permuted scales and one with block-order scales, timed in alternating
@@ -673,12 +789,17 @@ def run_sweep(args):
     if want("scale_layout_decode_b32_sq1_h128_topk2048_R352"):
         run_scale_layout(args, dev, iters, flush)
     # write path (quantize-append of 65,536 tokens into a 262,144-slot pool), 352-byte records and
-    # the 656-byte fp8 records they are compared with
+    # the 656-byte fp8 records they are compared with; then the fused producer
     for R in (352, 656):
         ww = synth.write_path(seed=0, record_bytes=R)
-        if not want(ww.name):
-            continue
-        run_write(ww, dev, iters, flush, hbm, peak_src)
+        if want(ww.name):
+            print(json.dumps({"sweep": True, "workload": ww.name, **measure_write(ww, dev, iters, flush, peaks),
+                              "peaks": peak_src, **oracle_append_rate(ww)}), flush=True)
+    pw = synth.producer_inputs(seed=0, record_bytes=352)
+    if want("norm_rope_" + pw.write.name):
+        print(json.dumps({"sweep": True, "workload": "norm_rope_" + pw.write.name,
+                          **measure_write(pw.write, dev, iters, flush, peaks, producer=pw), "peaks": peak_src}),
+              flush=True)
 
 
 def run_scale_layout(args, dev, iters, flush):
@@ -716,30 +837,6 @@ def run_scale_layout(args, dev, iters, flush):
     torch.cuda.empty_cache()
 
 
-def run_write(ww, dev, iters, flush, hbm, peak_src):
-    import nvfp4_kv_cache_sparse_gb300 as lib
-    cache = torch.full((ww.num_slots, ww.record_bytes), ww.fill_byte, dtype=torch.uint8, device=dev)
-    lat, rope, slots = ww.latent.to(dev), ww.rope.to(dev), ww.slot_mapping.to(dev)
-
-    def append():
-        lib.quantize_append(lat, rope, slots, cache)
-
-    for _ in range(3):
-        append()
-    torch.cuda.synchronize()
-    warm = _time_calls(append, iters)
-    cold = _time_calls(append, iters, flush)
-    bytes_ = ww.T * (512 * 2 + 64 * 2 + 8 + ww.record_bytes)
-    t_roof = bytes_ / (hbm * 1e9)
-    print(json.dumps({"sweep": True, "workload": ww.name, "kind": "quantize_append", "tokens": ww.T,
-                      "us_per_call_warm": warm * 1e6, "us_per_call_cold": cold * 1e6,
-                      "tokens_per_s_cold": ww.T / cold, "achieved_gbs_cold": bytes_ / cold / 1e9,
-                      "roofline_us": t_roof * 1e6, "roofline_frac_cold": t_roof / cold, "bound": "hbm",
-                      "algorithmic_bytes": bytes_, "peaks": peak_src, **oracle_append_rate(ww)}), flush=True)
-    del cache
-    torch.cuda.empty_cache()
-
-
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -749,6 +846,11 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-rows", type=int, default=4)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-rows-1core", type=int, default=2,
+                    help="query rows of the single-core oracle sample in cpu_baseline")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="leave out the per-configuration measurements of the N=1 line")
+    ap.add_argument("--config-iters", type=int, default=20)
     ap.add_argument("--sweep", action="store_true",
                     help="time every workload configuration (decode and write path), one JSON line each")
     ap.add_argument("--sweep-iters", type=int, default=20)

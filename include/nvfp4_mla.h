@@ -159,6 +159,18 @@ NVFP4_MLA_API int nvfp4_sparse_mla_decode_workspace_size(int32_t batch, int32_t 
                                                          int32_t num_splits, size_t* bytes);
 
 /*
+ * How a decode of this shape runs on the current device (no launch, no device memory): the split
+ * count it uses (num_splits, or the library's choice when 0) and how many kernels one call
+ * launches (1: the decode grid alone, which also merges its 2-4 splits per row when they share a
+ * cluster; 2: decode grid + merge grid; 0: nothing to do). Errors as ..._workspace_size, plus
+ * NVFP4_MLA_ERR_UNSUPPORTED without a usable sm_103 device. (A service of this library; the pages
+ * have no counterpart.)
+ */
+NVFP4_MLA_API int nvfp4_sparse_mla_decode_plan(int32_t batch, int32_t s_q, int32_t h_q, int32_t topk,
+                                               int32_t record_bytes, int32_t num_splits, int32_t* splits,
+                                               int32_t* kernels);
+
+/*
  * Sparse MLA decode (read side).
  *   q            bf16 [batch, s_q, h_q, 576], contiguous, 16-byte aligned. Dims [0,512) are
  *                the NoPE (latent) part, [512,576) the RoPE part.

@@ -38,6 +38,7 @@ EXPORTED = (
     "nvfp4_mla_quantize_append",
     "nvfp4_mla_norm_rope_quantize_append",
     "nvfp4_sparse_mla_decode_workspace_size",
+    "nvfp4_sparse_mla_decode_plan",
     "nvfp4_sparse_mla_decode",
     "nvfp4_sparse_mla_decode_no_alloc",
     "nvfp4_mla_status_string",
@@ -77,6 +78,8 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
                                                         P, P]
     lib.nvfp4_sparse_mla_decode_workspace_size.restype = ctypes.c_int
     lib.nvfp4_sparse_mla_decode_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32, ctypes.POINTER(sz)]
+    lib.nvfp4_sparse_mla_decode_plan.restype = ctypes.c_int
+    lib.nvfp4_sparse_mla_decode_plan.argtypes = [i32, i32, i32, i32, i32, i32, ctypes.POINTER(i32), ctypes.POINTER(i32)]
     lib.nvfp4_sparse_mla_decode.restype = ctypes.c_int
     lib.nvfp4_sparse_mla_decode.argtypes = [P, P, i64, i32, P, i32, i32, i32, i32, f32, P, P, P, i32, P, sz, P, P]
     lib.nvfp4_sparse_mla_decode_no_alloc.restype = ctypes.c_int
@@ -181,6 +184,15 @@ def workspace_size(batch: int, s_q: int, h_q: int, topk: int, record_bytes: int,
     st = load().nvfp4_sparse_mla_decode_workspace_size(batch, s_q, h_q, topk, record_bytes, num_splits, ctypes.byref(n))
     _check("nvfp4_sparse_mla_decode_workspace_size", st)
     return int(n.value)
+
+
+def decode_plan(batch: int, s_q: int, h_q: int, topk: int, record_bytes: int, num_splits: int = 0):
+    """(splits, kernels per call) of a decode of this shape on the current device."""
+    sp, k = ctypes.c_int32(0), ctypes.c_int32(0)
+    st = load().nvfp4_sparse_mla_decode_plan(batch, s_q, h_q, topk, record_bytes, num_splits, ctypes.byref(sp),
+                                             ctypes.byref(k))
+    _check("nvfp4_sparse_mla_decode_plan", st)
+    return int(sp.value), int(k.value)
 
 
 def sparse_mla_decode(q: torch.Tensor, cache: torch.Tensor, indices: torch.Tensor, sm_scale: float,

@@ -191,6 +191,29 @@ NVFP4_MLA_API int nvfp4_sparse_mla_decode_workspace_size(int32_t batch, int32_t 
     return NVFP4_MLA_OK;
 }
 
+NVFP4_MLA_API int nvfp4_sparse_mla_decode_plan(int32_t batch, int32_t s_q, int32_t h_q, int32_t topk,
+                                               int32_t record_bytes, int32_t num_splits, int32_t* splits,
+                                               int32_t* kernels) {
+    if (!splits || !kernels) return NVFP4_MLA_ERR_INVALID_ARG;
+    const int st = check_decode_shape(batch, s_q, h_q, topk, record_bytes, num_splits);
+    if (st != NVFP4_MLA_OK) return st;
+    const int64_t rows = static_cast<int64_t>(batch) * s_q;
+    int status = NVFP4_MLA_OK;
+    const int sms = device_sm_count(&status);
+    if (sms <= 0) return status;
+    const int sp = num_splits > 0 ? num_splits : auto_splits(rows, topk, sms);
+    nvfp4mla::DecodeArgs d;
+    d.record_bytes = record_width(record_bytes);
+    d.block_scales = block_scales(record_bytes);
+    d.rows = static_cast<int>(rows);
+    d.h_q = h_q;
+    d.topk = topk;
+    d.splits = sp;
+    *splits = sp;
+    *kernels = rows == 0 ? 0 : (sp == 1 || nvfp4mla::decode_pair_merges(d)) ? 1 : 2;
+    return NVFP4_MLA_OK;
+}
+
 NVFP4_MLA_API int nvfp4_sparse_mla_decode(const void* q, const uint8_t* cache, int64_t num_slots, int32_t record_bytes,
                                           const int32_t* indices, int32_t batch, int32_t s_q, int32_t h_q,
                                           int32_t topk, float sm_scale, const float* attn_sink, void* out, float* lse,

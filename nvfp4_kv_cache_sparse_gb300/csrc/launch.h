@@ -60,6 +60,9 @@ cudaError_t launch_sparse_decode(const DecodeArgs& a, cudaStream_t stream);
 // The CTA-pair decode with shared MMAs (sparse_decode_pair.cu): 128 heads, 352- or 432-byte records.
 bool decode_pair_supported(const DecodeArgs& a);
 int decode_pair_keys_per_split(int topk, int splits);
+// Whether a decode of these arguments merges its splits inside the decode grid (2-4 splits per
+// row in one cluster, the whole grid resident at once).
+bool decode_pair_merges(const DecodeArgs& a);
 // merged: set when the grid merges the splits itself (2-4 splits per row in one cluster).
 cudaError_t launch_decode_pair(const DecodeArgs& a, cudaStream_t stream, bool* merged);
 // The split merge (out, lse from the f16 partials), launched as a programmatic dependent.

@@ -982,6 +982,57 @@ int decode_pair_keys_per_split(int topk, int splits) {
     return (per + pairdec::kTile - 1) / pairdec::kTile * pairdec::kTile;
 }
 
+// How many clusters of 2 * splits CTAs of this kernel variant fit on the current device at once
+// (0: none), asked once per variant, split count and device.
+int pair_clusters_fit(int record_bytes, bool block_scales, int splits) {
+    using namespace pairdec;
+    if (splits < 1 || splits > kMaxClusterSplits) return 0;
+    static std::atomic<int> fits[3][kMaxClusterSplits + 1][8];   // 0 unknown, else 1 + clusters
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    const int variant = record_bytes == 432 ? 2 : block_scales ? 1 : 0;
+    std::atomic<int>& known = fits[variant][splits][dev & 7];
+    int state = known.load(std::memory_order_relaxed);
+    if (state == 0) {
+        const auto kernel = record_bytes == 432 ? decode_pair_kernel<432, false>
+                            : block_scales      ? decode_pair_kernel<352, true>
+                                                : decode_pair_kernel<352, false>;
+        const cudaError_t err = record_bytes == 432 ? prepare_kernel<432, false>()
+                                : block_scales      ? prepare_kernel<352, true>()
+                                                    : prepare_kernel<352, false>();
+        int clusters = 0;
+        if (err == cudaSuccess) {
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(2u * static_cast<unsigned>(splits));
+            cfg.blockDim = dim3(kThreads);
+            cfg.dynamicSmemBytes = record_bytes == 432 ? kSmemAlloc<432> : kSmemAlloc<352>;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = 2u * static_cast<unsigned>(splits);
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            if (cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg) != cudaSuccess) clusters = 0;
+        }
+        (void)cudaGetLastError();
+        state = 1 + (clusters > 0 ? clusters : 0);
+        known.store(state, std::memory_order_relaxed);
+    }
+    return state - 1;
+}
+
+// All splits of a row in one cluster when there are 2-4 of them and such clusters fit on this
+// GPU all at once (a second wave of large clusters would leave SMs idle): the kernel then merges
+// them itself and no merge grid follows.
+bool decode_pair_merges(const DecodeArgs& d) {
+    if (!decode_pair_supported(d) || d.splits < 2 || d.splits > pairdec::kMaxClusterSplits) return false;
+    return static_cast<int64_t>(pair_clusters_fit(d.record_bytes, d.block_scales, d.splits)) >= d.rows;
+}
+
 cudaError_t launch_decode_pair(const DecodeArgs& d, cudaStream_t stream, bool* merged) {
     using namespace pairdec;
     KernelArgs a;
@@ -1019,33 +1070,10 @@ cudaError_t launch_decode_pair(const DecodeArgs& d, cudaStream_t stream, bool* m
     cfg.numAttrs = 2;
     // All splits of a row in one cluster when there are 2-4 of them and such clusters fit on this
     // GPU: the kernel then merges them itself and no merge grid follows.
-    a.merge = 0;
-    if (d.splits >= 2 && d.splits <= kMaxClusterSplits) {
-        attr[1].val.clusterDim.x = 2u * static_cast<unsigned>(d.splits);
-        attr[1].val.clusterDim.y = 1;
-        attr[1].val.clusterDim.z = 1;
-        // how many such clusters fit at once, asked once per kernel variant, cluster size and device
-        static std::atomic<int> fits[3][kMaxClusterSplits + 1][8];
-        int dev = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidValue;
-        const int variant = d.record_bytes == 432 ? 2 : d.block_scales ? 1 : 0;
-        std::atomic<int>& known = fits[variant][d.splits][dev & 7];
-        int state = known.load(std::memory_order_relaxed);   // 0 unknown, 1 none fits, else 2 + clusters that fit
-        if (state == 0) {
-            int clusters = 0;
-            state = cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg) == cudaSuccess && clusters > 0 ? clusters + 2 : 1;
-            (void)cudaGetLastError();
-            known.store(state, std::memory_order_relaxed);
-        }
-        // and only when the whole grid is resident at once (a second wave of large clusters would
-        // leave SMs idle)
-        a.merge = state >= 2 && static_cast<int64_t>(state - 2) >= d.rows ? 1 : 0;
-    }
-    if (!a.merge) {
-        attr[1].val.clusterDim.x = 2;
-        attr[1].val.clusterDim.y = 1;
-        attr[1].val.clusterDim.z = 1;
-    }
+    a.merge = decode_pair_merges(d) ? 1 : 0;
+    attr[1].val.clusterDim.x = a.merge ? 2u * static_cast<unsigned>(d.splits) : 2u;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
     *merged = a.merge != 0;
     err = cudaLaunchKernelEx(&cfg, kernel, a);
     if (err == cudaSuccess) err = cudaGetLastError();

@@ -37,3 +37,11 @@ def test_misaligned_and_unsupported_arguments_match_the_workspace_entry_point():
     args = [good, good, 100, 352, good, 2, 1, 96, 512, ctypes.c_float(0.1), None, good, good, 4]   # h_q 96
     assert cdll.nvfp4_sparse_mla_decode_no_alloc(*(args + [None, None])) == lib.ERR_UNSUPPORTED
     assert cdll.nvfp4_sparse_mla_decode(*(args + [None, 0, None, None])) == lib.ERR_UNSUPPORTED
+
+
+def test_decode_plan_checks_its_arguments_without_a_device():
+    cdll = lib.load(build_if_missing=True)
+    sp, k = ctypes.c_int32(0), ctypes.c_int32(0)
+    assert cdll.nvfp4_sparse_mla_decode_plan(1, 1, 128, 64, 352, 1, None, ctypes.byref(k)) == lib.ERR_INVALID_ARG
+    assert cdll.nvfp4_sparse_mla_decode_plan(1, 1, 96, 64, 352, 1, ctypes.byref(sp), ctypes.byref(k)) == lib.ERR_UNSUPPORTED
+    assert cdll.nvfp4_sparse_mla_decode_plan(1, 1, 128, 0, 352, 1, ctypes.byref(sp), ctypes.byref(k)) == lib.ERR_INVALID_ARG

@@ -95,3 +95,14 @@ def test_no_alloc_is_bit_identical_to_the_workspace_entry_point(record_bytes, sp
     assert int(status.item()) == 0
     assert torch.equal(out, ref_out)
     assert torch.equal(lse, ref_lse)
+
+
+def test_decode_plan_matches_the_launch_structure():
+    """One kernel per call when the splits merge inside the decode grid (2-4 splits, one wave of
+    clusters) or there is one split; two (decode + merge grid) otherwise."""
+    assert lib.decode_plan(32, 1, 128, 2048, 352, 1) == (1, 1)
+    assert lib.decode_plan(32, 1, 128, 2048, 352, 2) == (2, 1)
+    assert lib.decode_plan(32, 1, 128, 2048, 352, 8) == (8, 2)
+    assert lib.decode_plan(32, 1, 128, 2048, 352, 0)[0] >= 1
+    assert lib.decode_plan(4, 1, 64, 2048, 352, 2) == (2, 2)       # h_q 64: the merge grid follows
+    assert lib.decode_plan(0, 1, 128, 2048, 352, 2)[1] == 0
