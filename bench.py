@@ -44,7 +44,7 @@ PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM bytes (read + write) of one decode_pair_kernel launch on this workload, from an ncu
 # capture (dram__bytes_read.sum + dram__bytes_write.sum), keyed by the hash of the decode code
 # (comments removed) it was taken with; reported as null once that code changes.
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {"ae449942f712": 34266368 + 48896}
 DECODE_CALLS_TIMED = 128   # the decode call alone: 16 laps of 8 back-to-back calls
 
 
@@ -837,6 +837,43 @@ def run_scale_layout(args, dev, iters, flush):
     torch.cuda.empty_cache()
 
 
+def run_profile_config(name: str):
+    """Four calls (three warm-up, then the one an ncu capture with `-s 3 -c 1` takes) of one
+    configuration's kernel, untimed: the command the summaries under profiles/ were taken with."""
+    import nvfp4_kv_cache_sparse_gb300 as lib
+    from synth.pool import fill_pool
+    lib.load()
+    dev = torch.device("cuda", 0)
+    if name in ("decode", "longctx", "varlen"):
+        make = {"decode": synth.batch_decode, "longctx": synth.long_context, "varlen": synth.varlen_decode}[name]
+        # varlen at B = 32 (a 0.78 GB pool) instead of 128 (3 GB), to keep the profiler's replays small
+        w = make(seed=0, B=32) if name == "varlen" else make(seed=0)
+        cache = fill_pool(lib.quantize_append, w.num_slots, w.record_bytes, w.pool_seed, dev)
+        q, idx = w.q.to(dev), w.indices.to(dev)
+        sink = None if w.attn_sink is None else w.attn_sink.to(dev)
+
+        def call():
+            lib.sparse_mla_decode(q, cache, idx, w.sm_scale, attn_sink=sink)
+    else:
+        pw = synth.producer_inputs(seed=0, record_bytes=352)
+        ww = pw.write if name == "producer" else synth.write_path(seed=0, record_bytes=352)
+        cache = torch.full((ww.num_slots, 352), ww.fill_byte, dtype=torch.uint8, device=dev)
+        lat, rope, slots = ww.latent.to(dev), ww.rope.to(dev), ww.slot_mapping.to(dev)
+        nw, pos = pw.norm_weight.to(dev), pw.positions.to(dev)
+        cos, sin = pw.cos_table.to(dev), pw.sin_table.to(dev)
+
+        def call():
+            if name == "append":
+                lib.quantize_append(lat, rope, slots, cache)
+            else:
+                lib.norm_rope_quantize_append(lat, nw, pw.eps, rope, pos, cos, sin, pw.rotate_half, slots, cache)
+    torch.cuda.synchronize()
+    for _ in range(4):
+        call()
+    torch.cuda.synchronize()
+    print(json.dumps({"profile_config": name, "calls": 4}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -856,7 +893,12 @@ def main():
     ap.add_argument("--sweep-iters", type=int, default=20)
     ap.add_argument("--sweep-filter", default=None,
                     help="with --sweep: time only the configurations whose name contains this string")
+    ap.add_argument("--profile-config", choices=["decode", "longctx", "varlen", "append", "producer"], default=None,
+                    help="make four untimed calls of one configuration (for ncu captures) and exit")
     args = ap.parse_args()
+    if args.profile_config:
+        run_profile_config(args.profile_config)
+        return
     if args.sweep:
         run_sweep(args)
         return
