@@ -692,7 +692,7 @@ def measure_decode(w, dev, iters, flush, peaks):
     return res
 
 
-def measure_write(ww, dev, iters, flush, peaks, producer=None):
+def measure_write(ww, dev, iters, flush, peaks, producer=None, flush_clean=None):
     """The append (or, with a producer workload, the fused norm + rotary + append and the unfused
     path it replaces: torch norm and rotation into a bf16 intermediate, then the append)."""
     import nvfp4_kv_cache_sparse_gb300 as lib
@@ -727,11 +727,17 @@ def measure_write(ww, dev, iters, flush, peaks, producer=None):
         warm = _time_calls(call, iters)
         cold = _time_calls(call, iters, flush)
         unf = _time_calls(unfused, max(5, iters // 4), flush) if producer is not None else None
+        clean = _time_calls(call, iters, flush_clean) if flush_clean is not None else None
     t_roof = bytes_ / (hbm * 1e9)
     res = {"kind": "quantize_append" if producer is None else "norm_rope_quantize_append", "tokens": ww.T,
            "us_per_call_warm": warm * 1e6, "us_per_call_cold": cold * 1e6, "tokens_per_s_cold": ww.T / cold,
            "achieved_gbs_cold": bytes_ / cold / 1e9, "roofline_us": t_roof * 1e6, "roofline_frac_cold": t_roof / cold,
            "bound": "hbm", "algorithmic_bytes": bytes_, "calls_timed": iters, "clocks": sampler.summary()}
+    if clean is not None:
+        # cold with a clean L2: the flush reads a 512 MB buffer instead of writing it, so no dirty
+        # lines of the flush are written back to HBM while the call runs
+        res["us_per_call_cold_clean_l2"] = clean * 1e6
+        res["roofline_frac_cold_clean_l2"] = t_roof / clean
     if unf is not None:
         res["unfused_us_per_call_cold"] = unf * 1e6
         res["unfused_path"] = "torch rms_norm and rotation into a bf16 intermediate, then quantize_append"
@@ -745,18 +751,23 @@ def measure_configs(dev, iters) -> dict:
     roofline fraction and the clocks seen while timing it (the default line carries them)."""
     peaks, _ = load_peaks()
     scrub = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    scrub_i = scrub.view(torch.int32)
 
     def flush():
         scrub.fill_(1)
+
+    def flush_clean():
+        scrub_i.sum()
 
     res = {}
     for name, make in DECODE_CONFIGS:
         res[name] = measure_decode(make(), dev, iters, flush, peaks)
     for R in (352, 656):
         ww = synth.write_path(seed=0, record_bytes=R)
-        res[ww.name] = measure_write(ww, dev, iters, flush, peaks)
+        res[ww.name] = measure_write(ww, dev, iters, flush, peaks, flush_clean=flush_clean)
     pw = synth.producer_inputs(seed=0, record_bytes=352)
-    res["norm_rope_" + pw.write.name] = measure_write(pw.write, dev, iters, flush, peaks, producer=pw)
+    res["norm_rope_" + pw.write.name] = measure_write(pw.write, dev, iters, flush, peaks, producer=pw,
+                                                      flush_clean=flush_clean)
     del scrub
     torch.cuda.empty_cache()
     return res

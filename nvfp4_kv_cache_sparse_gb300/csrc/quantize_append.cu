@@ -21,9 +21,9 @@
 //
 // Design: one warp per token, lane g owns the 16-value group g. The group maximum is taken on
 // the |bf16| bit patterns (non-negative floats order like integers) with packed 16-bit maxima,
-// so no shuffles are needed. The record is assembled in a per-warp shared-memory stage and
-// written with 16-byte stores (22 lanes for 352 B, 27 for 432 B, 41 chunks over 32 lanes for
-// 656 B), so each record is one contiguous burst.
+// so no shuffles are needed. An NVFP4 record is written in place, each store instruction of
+// the warp covering one contiguous field of it; an fp8 record is assembled in a per-warp
+// shared-memory stage and written with 16-byte stores (41 chunks over 32 lanes).
 //
 // Exactness of x / s without a division per value: s is an e4m3 value (<= 4 significant bits)
 // and x a bf16 value (<= 8), so the exact quotient x/s is either exactly one of the e2m1 tie
@@ -198,6 +198,7 @@ quantize_append_kernel(const uint16_t* __restrict__ latent, int64_t latent_strid
                 if (lane == 0 && dev_status != nullptr) atomicOr(dev_status, 0x1u);
                 continue;
             }
+            uint8_t* const dst = cache + slot[u] * R;   // NVFP4 records are written in place (below)
             // ---- NoPE group `lane`: 16 bf16 values
             uint32_t w[8] = {va[u].x, va[u].y, va[u].z, va[u].w, vb[u].x, vb[u].y, vb[u].z, vb[u].w};
             uint32_t rwv = rw[u];
@@ -276,33 +277,43 @@ quantize_append_kernel(const uint16_t* __restrict__ latent, int64_t latent_strid
             uint32_t packed[2] = {0u, 0u};
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
-                const float q0 = round_to_12_bits(bf16_lo(w[k]) * inv_s);
-                const float q1 = round_to_12_bits(bf16_hi(w[k]) * inv_s);
+                // both products with one f32x2 FMA (addend -0, so that -0 stays -0)
+                float q0, q1;
+                asm("{\n .reg .b64 x, s, z, r;\n mov.b64 x, {%2, %3};\n mov.b64 s, {%4, %4};\n mov.b64 z, {%5, %5};\n"
+                    " fma.rn.f32x2 r, x, s, z;\n mov.b64 {%0, %1}, r;\n}\n"
+                    : "=f"(q0), "=f"(q1)
+                    : "f"(bf16_lo(w[k])), "f"(bf16_hi(w[k])), "f"(inv_s), "f"(-0.0f));
+                q0 = round_to_12_bits(q0);
+                q1 = round_to_12_bits(q1);
                 const uint32_t byte = e2m1x2_rn_sat(q1, q0);              // even element -> low nibble
                 packed[k >> 2] = (k & 3) ? __byte_perm(packed[k >> 2], byte, (k & 3) == 1 ? 0x3240u
                                                                             : (k & 3) == 2 ? 0x3410u
                                                                                            : 0x4210u)
                                          : byte;
             }
-            *reinterpret_cast<uint2*>(rec + 8 * lane) = make_uint2(packed[0], packed[1]);
+            // each store instruction of the warp covers one contiguous run of the record (codes 256 B,
+            // scales 32 B, RoPE 64 or 128 B, pad 16 B), so the record reaches L2 as whole lines
+            *reinterpret_cast<uint2*>(dst + 8 * lane) = make_uint2(packed[0], packed[1]);
 
             // ---- RoPE: lane owns elements 2*lane and 2*lane+1
             if constexpr (R == 352) {
-                rec[kBlk ? 320 + lane : 320 + 8 * (lane & 3) + (lane >> 2)] = static_cast<uint8_t>(sbyte);
+                dst[kBlk ? 320 + lane : 320 + 8 * (lane & 3) + (lane >> 2)] = static_cast<uint8_t>(sbyte);
                 const uint32_t c = e4m3x2_signed(bf16_hi(rwv), bf16_lo(rwv));
-                *reinterpret_cast<uint16_t*>(rec + 256 + 2 * lane) = static_cast<uint16_t>(c);
+                *reinterpret_cast<uint16_t*>(dst + 256 + 2 * lane) = static_cast<uint16_t>(c);
             } else {
-                rec[256 + lane] = static_cast<uint8_t>(sbyte);
-                *reinterpret_cast<uint32_t*>(rec + 304 + 4 * lane) = rwv;
-                if (lane < 4) *reinterpret_cast<uint32_t*>(rec + 288 + 4 * lane) = 0u;
+                dst[256 + lane] = static_cast<uint8_t>(sbyte);
+                *reinterpret_cast<uint32_t*>(dst + 304 + 4 * lane) = rwv;
+                if (lane < 4) *reinterpret_cast<uint32_t*>(dst + 288 + 4 * lane) = 0u;
             }
             }
-            __syncwarp();
-            for (int c = lane; c < R / 16; c += 32) {
-                const uint4 v = reinterpret_cast<const uint4*>(rec)[c];
-                reinterpret_cast<uint4*>(cache + slot[u] * R)[c] = v;
+            if constexpr (R == 656) {   // the fp8 record goes out from its stage as 16-byte stores
+                __syncwarp();
+                for (int c = lane; c < R / 16; c += 32) {
+                    const uint4 v = reinterpret_cast<const uint4*>(rec)[c];
+                    reinterpret_cast<uint4*>(dst)[c] = v;
+                }
+                __syncwarp();
             }
-            __syncwarp();
         }
         cur = nxt;
     }
