@@ -16,7 +16,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libnvfp4mla.so")
-SOURCES = ["api.cu", "quantize_append.cu", "sparse_decode.cu", "sparse_decode_pair.cu", "decode_no_alloc.cu"]
+SOURCES = ["api.cu", "quantize_append.cu", "sparse_decode.cu", "sparse_decode_pair.cu", "sparse_decode_h64.cu",
+           "decode_no_alloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

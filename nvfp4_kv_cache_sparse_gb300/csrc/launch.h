@@ -65,6 +65,11 @@ int decode_pair_keys_per_split(int topk, int splits);
 bool decode_pair_merges(const DecodeArgs& a);
 // merged: set when the grid merges the splits itself (2-4 splits per row in one cluster).
 cudaError_t launch_decode_pair(const DecodeArgs& a, cudaStream_t stream, bool* merged);
+// The transposed-score decode for 64 heads on one SM (sparse_decode_h64.cu): 352- or 432-byte
+// records.
+bool decode_h64_supported(const DecodeArgs& a);
+int decode_h64_keys_per_split(int topk, int splits);
+cudaError_t launch_decode_h64(const DecodeArgs& a, cudaStream_t stream);
 // The split merge (out, lse from the f16 partials), launched as a programmatic dependent.
 cudaError_t launch_split_merge(const DecodeArgs& a, cudaStream_t stream);
 // One time-bounded mbarrier wait that runs out (see nvfp4_mla_selftest_wait_timeout).

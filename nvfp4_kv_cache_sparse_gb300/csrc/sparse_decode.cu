@@ -1187,6 +1187,8 @@ cudaError_t launch_sparse_decode(const DecodeArgs& d, cudaStream_t stream) {
     bool merged = false;   // the decode grid merged the splits itself
     if (decode_pair_supported(d)) {
         err = launch_decode_pair(d, stream, &merged);
+    } else if (decode_h64_supported(d)) {
+        err = launch_decode_h64(d, stream);
     } else {
         KernelArgs a;
         if (!encode_cache_map(&a.tmap, d.cache, d.num_slots, d.record_bytes)) return cudaErrorInvalidValue;

@@ -52,6 +52,7 @@
 #include <atomic>
 #include <cstdint>
 
+#include "dequant.cuh"
 #include "launch.h"
 #include "sm103_ptx.cuh"
 
@@ -147,14 +148,6 @@ struct KernelArgs {
                               // merges their partials into out and lse after the whole cluster is done
 };
 
-__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t threads) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
-}
-
-__device__ __forceinline__ uint32_t swz(int row, int chunk) {
-    return static_cast<uint32_t>((row >> 3) * 1024 + (row & 7) * 128 + ((chunk ^ (row & 7)) << 4));
-}
-
 __device__ __forceinline__ void set_abort(Ctl* ctl, uint32_t* status) {
     if (atomicExch(&ctl->abort, 1u) == 0u && status != nullptr) atomicOr(status, 0x4u);
 }
@@ -195,58 +188,6 @@ __device__ __forceinline__ void signal_leader(Ctl* ctl, uint64_t* bar, int crank
     } else {
         st_async_b32(mapa_shared(smem_addr(&ctl->sig_sink), leader), 0u, mapa_shared(smem_addr(bar), leader));
     }
-}
-
-__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
-    const __half2 v = __floats2half2_rn(lo, hi);
-    return *reinterpret_cast<const uint32_t*>(&v);
-}
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<const uint32_t*>(&v);
-}
-
-// e4m3 scale byte -> (s, s) as f16x2 (exact).
-__device__ __forceinline__ __half2 scale_half2(uint32_t sbyte) {
-    uint32_t h;
-    const uint16_t in = static_cast<uint16_t>(sbyte | (sbyte << 8));
-    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(in));
-    return *reinterpret_cast<__half2*>(&h);
-}
-
-// Eight e2m1 codes (one word, low nibble first) times a scale -> four f16x2 words (exact).
-__device__ __forceinline__ uint4 dq8(uint32_t w, __half2 s2) {
-    uint32_t h[4];
-    asm("{\n"
-        "  .reg .b8 a, b, c, d;\n"
-        "  mov.b32 {a, b, c, d}, %4;\n"
-        "  cvt.rn.f16x2.e2m1x2 %0, a;\n"
-        "  cvt.rn.f16x2.e2m1x2 %1, b;\n"
-        "  cvt.rn.f16x2.e2m1x2 %2, c;\n"
-        "  cvt.rn.f16x2.e2m1x2 %3, d;\n"
-        "}\n"
-        : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
-        : "r"(w));
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        const __half2 p = __hmul2(*reinterpret_cast<const __half2*>(&h[k]), s2);
-        h[k] = *reinterpret_cast<const uint32_t*>(&p);
-    }
-    return make_uint4(h[0], h[1], h[2], h[3]);
-}
-
-// Four e4m3 codes -> two f16x2 words (exact).
-__device__ __forceinline__ uint2 e4m3x4_to_f16(uint32_t w) {
-    uint32_t a, b;
-    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(a) : "h"(static_cast<uint16_t>(w)));
-    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(b) : "h"(static_cast<uint16_t>(w >> 16)));
-    return make_uint2(a, b);
-}
-
-// Byte q of each word of w, low word first.
-__device__ __forceinline__ uint32_t gather_byte4(const uint4& w, int q) {
-    const uint32_t sel = static_cast<uint32_t>(q) | (static_cast<uint32_t>(q + 4) << 4);
-    return __byte_perm(__byte_perm(w.x, w.y, sel), __byte_perm(w.z, w.w, sel), 0x5410);
 }
 
 // V row of one key: the four blocks 4c + q (c = 4 half + cl) into V block cl, chunks 2q, 2q + 1.

@@ -118,13 +118,14 @@ def test_edge_rows_empty_single_duplicate_out_of_range():
         assert np.all(o[0] == 0) and np.all(np.isneginf(lse[0].cpu().numpy()))
 
 
+@pytest.mark.parametrize("H", [64, 128])
 @pytest.mark.parametrize("e", [-30, -12, 0, 20])
-def test_query_magnitudes_outside_the_f16_range(e):
+def test_query_magnitudes_outside_the_f16_range(e, H):
     """Queries of magnitude 2^e with sm_scale 2^-e / 24 give ordinary logits: q enters the
     tensor core unchanged at any magnitude (tiny rows, rows above the f16 maximum, a zero head,
     and a head whose odd dims are 2^-20 of the rest)."""
-    rng = np.random.default_rng(40 + e)
-    B, H, topk, n_slots = 2, 128, 150, 400
+    rng = np.random.default_rng(40 + e + H)
+    B, topk, n_slots = 2, 150, 400
     q = rng.standard_normal((B, 1, H, 576)).astype(np.float32)
     q[:, :, 5] = 0.0
     q[:, :, 7, 1::2] *= 2.0 ** -20
@@ -138,9 +139,10 @@ def test_query_magnitudes_outside_the_f16_range(e):
         assert np.allclose(lse.cpu().numpy()[:, :, 5], math.log(topk), atol=1e-4)
 
 
-def test_zero_query_is_mean_of_values_and_splits_agree():
+@pytest.mark.parametrize("H", [64, 128])
+def test_zero_query_is_mean_of_values_and_splits_agree(H):
     rng = np.random.default_rng(10)
-    q = np.zeros((2, 1, 128, 576), dtype=np.float32)
+    q = np.zeros((2, 1, H, 576), dtype=np.float32)
     idx = np.stack([rng.choice(1000, size=512, replace=False) for _ in range(2)]).reshape(2, 1, 512).astype(np.int32)
     outs = []
     for splits in (1, 2, 4, 8):
@@ -150,6 +152,24 @@ def test_zero_query_is_mean_of_values_and_splits_agree():
         outs.append(out.float().cpu())
     for o in outs[1:]:
         assert torch.allclose(o, outs[0], atol=1e-2, rtol=1e-2)
+
+
+@pytest.mark.parametrize("H,R,sm_scale", [(64, 352, 0.6), (64, 432, -0.45), (64, 352, 1.5), (128, 352, 0.6),
+                                           (128, 432, -0.45)])
+def test_reference_maximum_moves_on_later_tiles(H, R, sm_scale):
+    """|sm_scale| of order one spreads each head's logits over tens of log2 units, so its running
+    maximum keeps moving after the first tile (the rescale of O and of the row sums runs on later
+    tiles too, with both signs of sm_scale), over several tiles and a ragged last one."""
+    rng = np.random.default_rng(int(abs(sm_scale) * 100) + H + R)
+    B, topk, n_slots = 2, 900, 1200
+    q = rng.standard_normal((B, 1, H, 576)).astype(np.float32)
+    idx = np.stack([rng.choice(n_slots, size=topk, replace=False) for _ in range(B)]).reshape(B, 1, topk)
+    idx = idx.astype(np.int32)
+    idx[rng.random(idx.shape) < 0.05] = -1
+    for splits in (1, 3):
+        out, lse, ref_out, ref_lse, st = run_small(q, idx, R, n_slots, 21, sm_scale, rng.standard_normal(H), splits)
+        assert st == 0
+        assert_close(out, lse, ref_out, ref_lse)
 
 
 def test_many_splits_reused_dirty_workspace_is_deterministic():
