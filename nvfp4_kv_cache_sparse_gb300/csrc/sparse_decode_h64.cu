@@ -40,9 +40,9 @@
 //   0-7   softmax: warp w scores keys 32 (w & 3).. of a tile (its TMEM lane quadrant) for heads
 //         32 (w >> 2)..+31, and writes the RoPE rows of those keys for the next tile; q staging in
 //         the prologue; row sums, O^T / l and the output in the epilogue
-//   8-15  converters: four threads per key (keys j and j + 64), 16-dim blocks 4c + q of the key
-//         (c = 0..7, q = thread of the key); each thread holds the next tile's record bytes in
-//         registers while the current tile is scored
+//   8-15  converters: four threads per key (keys j and j + 64); thread q converts record bytes
+//         64c + 16q .. + 15 (c = 0..3: 16-dim blocks 8c + 2q, 8c + 2q + 1) and holds the next tile's
+//         bytes in registers while the current tile is scored
 //   16    MMA issuer (one elected thread) and tensor-memory owner
 // Every wait is bounded by time; on timeout the CTA sets NVFP4_MLA_DEV_TIMEOUT, stops issuing work,
 // drains what it issued and returns.
@@ -139,11 +139,6 @@ __device__ __forceinline__ bool wait_warp(Ctl* ctl, uint64_t* bar, uint32_t pari
 }
 
 // Read-only global loads that do not allocate in L1 (every record byte is used once per CTA).
-__device__ __forceinline__ uint2 ldg_stream8(const void* p) {
-    uint2 r;
-    asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p));
-    return r;
-}
 __device__ __forceinline__ uint4 ldg_stream16(const void* p) {
     uint4 r;
     asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
@@ -165,32 +160,41 @@ __device__ __forceinline__ float warp_max(float v) {
     return r;
 }
 
-// One key's share of a converter thread: the codes of its eight 16-dim blocks 4c + q (record
-// bytes 32c + 8q .. + 7) and the scale bytes that cover them.
+// One key's share of a converter thread q (0..3): record bytes 64c + 16q .. + 15 (c = 0..3), the codes
+// of 16-dim blocks 8c + 2q and 8c + 2q + 1, and the scale bytes of those blocks.
 template <int R, bool kBlkOrder>
 struct KeyRaw {
-    static constexpr bool kPermuted = R == 352 && !kBlkOrder;   // scale of block s at 320 + 8 (s & 3) + (s >> 2)
-    uint2 codes[8];
-    uint4 sc[kPermuted ? 1 : 2];   // permuted: .x, .y = bytes 320 + 8q ..; else the 32 scale bytes
+    // 352-byte records with the permuted placement (block s at 320 + 8 (s & 3) + (s >> 2)): the eight
+    // scale bytes of the thread's blocks lie in one 16-byte half of the field; otherwise all 32 bytes
+    static constexpr bool kPermuted = R == 352 && !kBlkOrder;
+    uint4 codes[4];
+    uint4 sc[kPermuted ? 1 : 2];
 
     __device__ __forceinline__ void load(const uint8_t* rec, int q) {
 #pragma unroll
-        for (int c = 0; c < 8; ++c) codes[c] = ldg_stream8(rec + 32 * c + 8 * q);
+        for (int c = 0; c < 4; ++c) codes[c] = ldg_stream16(rec + 64 * c + 16 * q);
         if constexpr (kPermuted) {
-            const uint2 s = ldg_stream8(rec + 320 + 8 * q);
-            sc[0] = make_uint4(s.x, s.y, 0u, 0u);
+            sc[0] = ldg_stream16(rec + 320 + 16 * (q & 1));
         } else {
             constexpr int sb = R == 352 ? 320 : 256;
             sc[0] = ldg_stream16(rec + sb);
             sc[1] = ldg_stream16(rec + sb + 16);
         }
     }
-    // byte c (c = 0..3 of the low word, 4..7 of the high word): scale of block 4c + q
-    __device__ __forceinline__ uint2 scales(int q) const {
-        if constexpr (kPermuted)
-            return make_uint2(sc[0].x, sc[0].y);
-        else
-            return make_uint2(gather_byte4(sc[0], q), gather_byte4(sc[1], q));
+    // byte 0: the scale of block 8c + 2q, byte 1: of block 8c + 2q + 1
+    __device__ __forceinline__ uint32_t scale_pair(int c, int q) const {
+        if constexpr (kPermuted) {
+            // block 8c + 2q at byte 16 (q & 1) + 2c + (q >> 1), the next block eight bytes further
+            const uint32_t wa = c < 2 ? sc[0].x : sc[0].y, wb = c < 2 ? sc[0].z : sc[0].w;
+            const uint32_t bi = static_cast<uint32_t>(2 * c + (q >> 1)) & 3u;
+            return __byte_perm(wa, wb, bi | ((bi + 4u) << 4));
+        } else {
+            // block s at byte s: bytes 2q, 2q + 1 of word 2c + (q >> 1)
+            const uint32_t w[8] = {sc[0].x, sc[0].y, sc[0].z, sc[0].w, sc[1].x, sc[1].y, sc[1].z, sc[1].w};
+            const uint32_t wv = (q >> 1) != 0 ? w[2 * c + 1] : w[2 * c];
+            const uint32_t lo = 2u * static_cast<uint32_t>(q & 1);
+            return __byte_perm(wv, 0u, lo | ((lo + 1u) << 4));
+        }
     }
 };
 
@@ -308,6 +312,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_h64_kernel(const __grid_co
         }
         int32_t cur_idx = index_at(0, key);
         load_rope(cur_idx);
+        int32_t next_idx = index_at(1, key);   // the index of the next tile's key, a tile ahead of its RoPE loads
         bool ok = wait_warp(ctl, &ctl->qload, 0, a.status);
         {
             const int hq = threadIdx.x >> 2;   // head 0..63
@@ -371,8 +376,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_h64_kernel(const __grid_co
         // Every softmax warp takes part in every named barrier below, also after a wait ran out
         // (then it only passes the barriers), so no warp can be left waiting on a missing one.
         for (int i = 0; i < n_tiles; ++i) {
-            const int32_t next_idx = index_at(i + 1, key);
             if (i + 1 < n_tiles) load_rope(next_idx);   // in flight while this tile is scored
+            const int32_t next2_idx = index_at(i + 2, key);
             float tmax = -INFINITY;
             if (ok) ok = wait_warp(ctl, &ctl->sfull, i & 1, a.status);
             if (ok) {
@@ -497,6 +502,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_h64_kernel(const __grid_co
             // ---- RoPE rows of the next tile (this tile's QK, which read the current ones, is done)
             valid = in_range(next_idx);
             if (i + 1 < n_tiles) store_rope(valid);
+            next_idx = next2_idx;
         }
 
         // ---- epilogue: row sums, O^T / l, out (or the split's partial) and lse
@@ -575,22 +581,30 @@ __global__ void __launch_bounds__(kThreads, 1) decode_h64_kernel(const __grid_co
         for (int k = 0; k < n_tiles; ++k) {
             const bool v0 = in_range(i0), v1 = in_range(i1);
             if (q == 0 && ((i0 >= 0 && !v0) || (i1 >= 0 && !v1)) && a.status != nullptr) atomicOr(a.status, 0x2u);
-            const uint2 s0 = r0.scales(q), s1 = r1.scales(q);
 #pragma unroll
             for (int b = 0; b < 4; ++b) {
-                // dims 128b .. 128b + 127 once the previous tile's PV has read them
+                // dims 128b .. 128b + 127 once the previous tile's PV has read them: 64-dim block
+                // 2b + (q >> 1), chunks 4 (q & 1) .. + 3 of each of the thread's two keys
                 if (k >= 1) ok = wait_warp(ctl, &ctl->pvblk[b], (k - 1) & 1, a.status);
                 if (!ok) break;
-#pragma unroll
-                for (int c = 2 * b; c < 2 * b + 2; ++c) {
-                    const uint32_t sh = 8 * (c & 3);
-                    const __half2 sa = scale_half2(((c < 4 ? s0.x : s0.y) >> sh) & 0xFFu);
-                    const __half2 sb = scale_half2(((c < 4 ? s1.x : s1.y) >> sh) & 0xFFu);
-                    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-                    sts_u128(k_s + c * kKBlk + swz(j, 2 * q), v0 ? dq8(r0.codes[c].x, sa) : z);
-                    sts_u128(k_s + c * kKBlk + swz(j, 2 * q + 1), v0 ? dq8(r0.codes[c].y, sa) : z);
-                    sts_u128(k_s + c * kKBlk + swz(j + 64, 2 * q), v1 ? dq8(r1.codes[c].x, sb) : z);
-                    sts_u128(k_s + c * kKBlk + swz(j + 64, 2 * q + 1), v1 ? dq8(r1.codes[c].y, sb) : z);
+                const uint32_t blk = k_s + (2 * b + (q >> 1)) * kKBlk;
+                const int ch0 = 4 * (q & 1);
+                const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+                {
+                    const uint32_t sp = r0.scale_pair(b, q);
+                    const __half2 sa = scale_half2(sp & 0xFFu), sb = scale_half2((sp >> 8) & 0xFFu);
+                    sts_u128(blk + swz(j, ch0), v0 ? dq8(r0.codes[b].x, sa) : z);
+                    sts_u128(blk + swz(j, ch0 + 1), v0 ? dq8(r0.codes[b].y, sa) : z);
+                    sts_u128(blk + swz(j, ch0 + 2), v0 ? dq8(r0.codes[b].z, sb) : z);
+                    sts_u128(blk + swz(j, ch0 + 3), v0 ? dq8(r0.codes[b].w, sb) : z);
+                }
+                {
+                    const uint32_t sp = r1.scale_pair(b, q);
+                    const __half2 sa = scale_half2(sp & 0xFFu), sb = scale_half2((sp >> 8) & 0xFFu);
+                    sts_u128(blk + swz(j + 64, ch0), v1 ? dq8(r1.codes[b].x, sa) : z);
+                    sts_u128(blk + swz(j + 64, ch0 + 1), v1 ? dq8(r1.codes[b].y, sa) : z);
+                    sts_u128(blk + swz(j + 64, ch0 + 2), v1 ? dq8(r1.codes[b].z, sb) : z);
+                    sts_u128(blk + swz(j + 64, ch0 + 3), v1 ? dq8(r1.codes[b].w, sb) : z);
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
