@@ -58,11 +58,15 @@ bool record_ok(int32_t r) {
 int record_width(int32_t r) { return r & 0xFFFF; }
 bool block_scales(int32_t r) { return (r & NVFP4_MLA_SCALES_BLOCK_ORDER) != 0; }
 
-// One CTA per (row, split, value half) and one CTA per SM: aim for one full wave.
-int auto_splits(int64_t rows, int32_t topk, int sm_count) {
-    const int64_t ctas_per_split = rows * 2;
+// One CTA per SM: aim for one full wave. The 64-head decode of NVFP4 records runs one CTA per
+// (row, split), the other decodes two; the NVFP4 decodes take keys in tiles of 128, the fp8 one 64.
+int auto_splits(int64_t rows, int32_t topk, int sm_count, int32_t h_q, int32_t record_bytes) {
+    const int r = record_width(record_bytes);
+    const bool nvfp4 = r == 352 || r == 432;
+    const int64_t ctas_per_split = rows * (nvfp4 && h_q == 64 ? 1 : 2);
+    const int tile = nvfp4 ? 2 * kDecodeTile : kDecodeTile;
     int64_t s = ctas_per_split >= sm_count ? 1 : sm_count / ctas_per_split;
-    const int64_t max_by_keys = (topk + kDecodeTile - 1) / kDecodeTile;
+    const int64_t max_by_keys = (topk + tile - 1) / tile;
     if (s > max_by_keys) s = max_by_keys;
     if (s > kMaxSplits) s = kMaxSplits;
     if (s < 1) s = 1;
@@ -185,7 +189,7 @@ NVFP4_MLA_API int nvfp4_sparse_mla_decode_workspace_size(int32_t batch, int32_t 
         int status = NVFP4_MLA_OK;
         const int sms = device_sm_count(&status);
         if (sms <= 0) return status;
-        splits = auto_splits(rows, topk, sms);
+        splits = auto_splits(rows, topk, sms, h_q, record_bytes);
     }
     *bytes = workspace_for(rows, h_q, splits);
     return NVFP4_MLA_OK;
@@ -201,7 +205,7 @@ NVFP4_MLA_API int nvfp4_sparse_mla_decode_plan(int32_t batch, int32_t s_q, int32
     int status = NVFP4_MLA_OK;
     const int sms = device_sm_count(&status);
     if (sms <= 0) return status;
-    const int sp = num_splits > 0 ? num_splits : auto_splits(rows, topk, sms);
+    const int sp = num_splits > 0 ? num_splits : auto_splits(rows, topk, sms, h_q, record_bytes);
     nvfp4mla::DecodeArgs d;
     d.record_bytes = record_width(record_bytes);
     d.block_scales = block_scales(record_bytes);
@@ -224,7 +228,7 @@ NVFP4_MLA_API int nvfp4_sparse_mla_decode(const void* q, const uint8_t* cache, i
     const int st = nvfp4mla::check_decode_call(q, cache, num_slots, record_bytes, indices, batch, s_q, h_q, topk,
                                                attn_sink, out, lse, num_splits, &rows, &sms);
     if (st != NVFP4_MLA_OK || rows == 0) return st;
-    const int splits = num_splits > 0 ? num_splits : auto_splits(rows, topk, sms);
+    const int splits = num_splits > 0 ? num_splits : auto_splits(rows, topk, sms, h_q, record_bytes);
     const size_t need = workspace_for(rows, h_q, splits);
     if (need > 0 && (!workspace || workspace_bytes < need || !aligned(workspace, 256))) return NVFP4_MLA_ERR_WORKSPACE;
 

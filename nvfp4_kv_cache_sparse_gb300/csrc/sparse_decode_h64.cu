@@ -578,6 +578,16 @@ __global__ void __launch_bounds__(kThreads, 1) decode_h64_kernel(const __grid_co
         if (in_range(i0)) r0.load(a.cache + static_cast<int64_t>(i0) * R, q);
         if (in_range(i1)) r1.load(a.cache + static_cast<int64_t>(i1) * R, q);
         int32_t n0 = index_at(1, j), n1 = index_at(1, j + 64);
+        int32_t m0 = index_at(2, j), m1 = index_at(2, j + 64);
+        // The records two tiles ahead go into L2 (the four threads of a key touch every 128-byte line
+        // of its record: points 64 apart), so that the register loads a tile ahead find them there.
+        auto prefetch_record = [&](int32_t v) {
+            if (in_range(v)) {
+                const uint8_t* rec = a.cache + static_cast<int64_t>(v) * R;
+                prefetch_l2(rec + min(128 * q, R - 1));
+                prefetch_l2(rec + min(128 * q + 64, R - 1));
+            }
+        };
         for (int k = 0; k < n_tiles; ++k) {
             const bool v0 = in_range(i0), v1 = in_range(i1);
             if (q == 0 && ((i0 >= 0 && !v0) || (i1 >= 0 && !v1)) && a.status != nullptr) atomicOr(a.status, 0x2u);
@@ -616,8 +626,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_h64_kernel(const __grid_co
             i1 = n1;
             if (in_range(i0)) r0.load(a.cache + static_cast<int64_t>(i0) * R, q);
             if (in_range(i1)) r1.load(a.cache + static_cast<int64_t>(i1) * R, q);
-            n0 = index_at(k + 2, j);
-            n1 = index_at(k + 2, j + 64);
+            prefetch_record(m0);
+            prefetch_record(m1);
+            n0 = m0;
+            n1 = m1;
+            m0 = index_at(k + 3, j);
+            m1 = index_at(k + 3, j + 64);
         }
     } else {
         // ======================= MMA issuer =======================
