@@ -44,7 +44,7 @@ PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM bytes (read + write) of one decode_pair_kernel launch on this workload, from an ncu
 # capture (dram__bytes_read.sum + dram__bytes_write.sum), keyed by the hash of the decode code
 # (comments removed) it was taken with; reported as null once that code changes.
-NCU_TRAFFIC = {"ae449942f712": 34266368 + 48896}
+NCU_TRAFFIC = {"f7a55f8541dd": 34268672 + 47104}
 DECODE_CALLS_TIMED = 128   # the decode call alone: 16 laps of 8 back-to-back calls
 
 

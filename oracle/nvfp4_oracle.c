@@ -293,8 +293,9 @@ void oracle_sparse_mla_decode(const uint16_t* q, const uint8_t* cache, int64_t n
                               const float* sink, const int64_t* tok_list, int64_t n_list,
                               double* out, double* lse, int threads) {
     if (tok_list == NULL) n_list = n_tok;
+    /* threads > 0: that many OpenMP threads for this call only; 0: every host core */
 #ifdef _OPENMP
-    if (threads > 0) omp_set_num_threads(threads);
+    const int n_threads = threads > 0 ? threads : omp_get_num_procs();
 #else
     (void)threads;
 #endif
@@ -311,7 +312,7 @@ void oracle_sparse_mla_decode(const uint16_t* q, const uint8_t* cache, int64_t n
             ++n_used;
         }
 #ifdef _OPENMP
-#pragma omp parallel for schedule(dynamic)
+#pragma omp parallel for schedule(dynamic) num_threads(n_threads)
 #endif
         for (int h = 0; h < h_q; ++h) {
             double* o = out + ((size_t)r * h_q + h) * 512;
@@ -491,7 +492,7 @@ void oracle_e4m3_decode_many(const uint8_t* c, int64_t n, double* out) {
 }
 int oracle_threads_available(void) {
 #ifdef _OPENMP
-    return omp_get_max_threads();
+    return omp_get_num_procs();
 #else
     return 1;
 #endif
