@@ -855,10 +855,13 @@ def run_profile_config(name: str):
     from synth.pool import fill_pool
     lib.load()
     dev = torch.device("cuda", 0)
-    if name in ("decode", "longctx", "varlen"):
-        make = {"decode": synth.batch_decode, "longctx": synth.long_context, "varlen": synth.varlen_decode}[name]
+    if name in ("decode", "longctx", "varlen", "tiny", "prefill", "fp8"):
+        make = {"decode": synth.batch_decode, "longctx": synth.long_context, "varlen": synth.varlen_decode,
+                "tiny": synth.tiny_decode, "prefill": synth.sparse_prefill, "fp8": synth.batch_decode}[name]
         # varlen at B = 32 (a 0.78 GB pool) instead of 128 (3 GB), to keep the profiler's replays small
         w = make(seed=0, B=32) if name == "varlen" else make(seed=0)
+        if name == "fp8":
+            w = dataclasses.replace(w, record_bytes=656)
         cache = fill_pool(lib.quantize_append, w.num_slots, w.record_bytes, w.pool_seed, dev)
         q, idx = w.q.to(dev), w.indices.to(dev)
         sink = None if w.attn_sink is None else w.attn_sink.to(dev)
@@ -904,7 +907,8 @@ def main():
     ap.add_argument("--sweep-iters", type=int, default=20)
     ap.add_argument("--sweep-filter", default=None,
                     help="with --sweep: time only the configurations whose name contains this string")
-    ap.add_argument("--profile-config", choices=["decode", "longctx", "varlen", "append", "producer"], default=None,
+    ap.add_argument("--profile-config", choices=["decode", "longctx", "varlen", "tiny", "prefill", "fp8", "append", "producer"],
+                    default=None,
                     help="make four untimed calls of one configuration (for ncu captures) and exit")
     args = ap.parse_args()
     if args.profile_config:
