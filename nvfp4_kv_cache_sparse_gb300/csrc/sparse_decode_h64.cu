@@ -19,7 +19,8 @@
 //     dequantized once, into one buffer, and serves both contractions.
 // Tensor memory: O^T 256 columns (block b: lanes = dims 128b.., columns = heads), S^T 64 columns
 // (lanes = keys), the RoPE rows of K 32 columns (lanes = keys), and each key lane's share of every
-// head's row sum l, 64 columns (kept there rather than in the softmax threads' registers).
+// head's row sum l, two buffers of 64 columns (kept there rather than in the softmax threads'
+// registers; a tile reads one and writes the other).
 // Shared memory: Q 72 KB, the K tile 128 KB (eight 64-dim blocks of 128 keys, 128B-swizzled), P^T
 // 16 KB (128 keys x 64 heads, heads contiguous: the MN-major B operand of the PV MMAs).
 // Pipeline. One buffer per operand. The converters refill K dims block b (128 dims) of tile k + 1
@@ -32,10 +33,12 @@
 // q_d K_d are the same numbers as with bf16 q; S^T column h comes out as 2^pre_h times the exact
 // score, which the softmax folds into its per-head scale. P is f16 (entries in [0, 2^8]).
 // Softmax. A lazy reference maximum m_h per head (log2 domain): P = 2^(z - m) and O, l accumulate
-// against m. A tile needs the reference to move only when some score exceeds m + 8; the softmax
-// warps vote on that once per tile (one barrier reduction) and only then reduce the tile's maxima
-// across keys (lanes) and rescale O^T. Masked keys (index -1 or out of range) get zero K rows and
-// P = 0: the thread that scores a key also loads its index.
+// against m. A tile needs the reference to move only when some score exceeds m + 8. One pass over a
+// key's scores writes P and the row sums against the current references and finds the largest
+// z - m; the softmax warps then vote once per tile (one barrier reduction), and only when a
+// reference has to move do they reduce the tile's maxima across keys (lanes), rescale O^T and redo
+// the pass. Masked keys (index -1 or out of range) get zero K rows and P = 0: the thread that
+// scores a key also loads its index.
 // Warp roles (kThreads = 544, 17 warps):
 //   0-7   softmax: warp w scores keys 32 (w & 3).. of a tile (its TMEM lane quadrant) for heads
 //         32 (w >> 2)..+31, and writes the RoPE rows of those keys for the next tile; q staging in
@@ -70,7 +73,7 @@ constexpr int kWarpMma = 16;
 constexpr uint32_t kColO = 0;              // O^T: 4 blocks of 64 columns
 constexpr uint32_t kColS = 256;            // S^T: 64 columns
 constexpr uint32_t kColR = 320;            // RoPE rows of K: 32 columns (64 16-bit values a lane)
-constexpr uint32_t kColL = 352;            // row-sum partials: 64 columns (lane = key lane, column = head)
+constexpr uint32_t kColL = 352;            // row-sum partials: two buffers of 64 columns (lane = key lane, column = head)
 constexpr int kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -375,32 +378,61 @@ __global__ void __launch_bounds__(kThreads, 1) decode_h64_kernel(const __grid_co
         const uint32_t p_row = sbase + kOffP + (key >> 3) * 1024 + (key & 7) * 128;   // this key's row of P^T
         // Every softmax warp takes part in every named barrier below, also after a wait ran out
         // (then it only passes the barriers), so no warp can be left waiting on a missing one.
+        // One pass over this key's scores: P^T row = 2^(z - m) in f16 (0 for a masked key) against the
+        // current references, the row sums l_new = alpha l_old + P (alpha = 1 unless `rescale`), and
+        // the largest z - m. P^T of the previous tile was read by its PV, which completed before this
+        // tile's QK did. The sums go to the other of two TMEM buffers, so that a tile whose vote
+        // moves a reference can redo the pass from the previous sums.
+        auto score = [&](uint32_t l_old, uint32_t l_new, bool rescale) -> float {
+            float tmax = -INFINITY;
+#pragma unroll 1
+            for (int half = 0; half < 2; ++half) {
+                uint32_t sv[16], lv[16];
+                tmem_ld16(lane_base + kColS + hb + 16 * half, sv);
+                tmem_ld16(lane_base + l_old + hb + 16 * half, lv);
+                tmem_wait_ld();
+#pragma unroll
+                for (int c2 = 0; c2 < 2; ++c2) {
+                    uint32_t pw[4];
+#pragma unroll
+                    for (int g2 = 0; g2 < 4; ++g2) {
+                        const int e = 8 * c2 + 2 * g2;     // column in sv / lv
+                        const int h = hb + 16 * half + e;  // heads h, h + 1
+                        const uint4 c = lds_u128(cm_s + 16 * (h >> 1));
+                        const float2 z = f32x2_unpack(f32x2_fma(f32x2_pack(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])),
+                                                                f32x2_pack(__uint_as_float(c.x), __uint_as_float(c.y)),
+                                                                f32x2_pack(__uint_as_float(c.z), __uint_as_float(c.w))));
+                        tmax = fmax3(tmax, z.x, z.y);
+                        const float p0 = valid ? ex2_approx(z.x) : 0.0f, p1 = valid ? ex2_approx(z.y) : 0.0f;
+                        uint64_t l2 = f32x2_pack(__uint_as_float(lv[e]), __uint_as_float(lv[e + 1]));
+                        if (rescale) {
+                            const uint2 al = lds_u64(alpha_s + 4 * h);
+                            l2 = f32x2_fma(l2, f32x2_pack(__uint_as_float(al.x), __uint_as_float(al.y)), f32x2_pack(p0, p1));
+                        } else {
+                            l2 = f32x2_add(l2, f32x2_pack(p0, p1));
+                        }
+                        const float2 ls = f32x2_unpack(l2);
+                        lv[e] = __float_as_uint(ls.x);
+                        lv[e + 1] = __float_as_uint(ls.y);
+                        pw[g2] = pack_f16x2(p0, p1);
+                    }
+                    sts_u128(p_row + (((4 * h2 + 2 * half + c2) ^ (key & 7)) << 4), make_uint4(pw[0], pw[1], pw[2], pw[3]));
+                }
+                tmem_st16(lane_base + l_new + hb + 16 * half, lv);
+            }
+            return valid ? tmax : -INFINITY;
+        };
         for (int i = 0; i < n_tiles; ++i) {
             if (i + 1 < n_tiles) load_rope(next_idx);   // in flight while this tile is scored
             const int32_t next2_idx = index_at(i + 2, key);
+            const uint32_t l_old = kColL + 64 * (i & 1), l_new = kColL + 64 * ((i + 1) & 1);
             float tmax = -INFINITY;
             if (ok) ok = wait_warp(ctl, &ctl->sfull, i & 1, a.status);
             if (ok) {
-                // S^T stays in tensor memory until the next QK, which waits for this tile's P^T, so
-                // each pass below reads it again instead of holding it in registers
-                tc_fence_after_sync();
                 // (tensor-memory loads and stores are warp-collective: every lane takes part, and a
                 // masked key only changes the values)
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    uint32_t sv[16];
-                    tmem_ld16(lane_base + kColS + hb + 16 * half, sv);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int g = 0; g < 8; ++g) {   // heads hb + 16 half + 2g, + 1: z - m
-                        const uint4 c = lds_u128(cm_s + 16 * ((hb >> 1) + 8 * half + g));
-                        const float2 t = f32x2_unpack(f32x2_fma(f32x2_pack(__uint_as_float(sv[2 * g]), __uint_as_float(sv[2 * g + 1])),
-                                                                f32x2_pack(__uint_as_float(c.x), __uint_as_float(c.y)),
-                                                                f32x2_pack(__uint_as_float(c.z), __uint_as_float(c.w))));
-                        tmax = fmax3(tmax, t.x, t.y);
-                    }
-                }
-                if (!valid) tmax = -INFINITY;
+                tc_fence_after_sync();
+                tmax = score(l_old, l_new, false);
             }
             // ---- does any head need a new reference? (one barrier reduction)
             if (bar_red_or(1, 256, tmax > kRescaleThreshold)) {
@@ -435,17 +467,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_h64_kernel(const __grid_co
                     sts_f32(alpha_s + 4 * (hb + lane), al);
                 }
                 named_bar_sync(1, 256);
-#pragma unroll 1
-                for (int half = 0; half < 2; ++half) {   // l *= alpha
-                    uint32_t lv[16];
-                    tmem_ld16(lane_base + kColL + hb + 16 * half, lv);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int e = 0; e < 16; ++e)
-                        lv[e] = __float_as_uint(__uint_as_float(lv[e]) * lds_f32(alpha_s + 4 * (hb + 16 * half + e)));
-                    tmem_st16(lane_base + kColL + hb + 16 * half, lv);
-                }
-                tmem_wait_st();
                 if (ok && i > 0) {
                     // O^T (dims 128b + key lane, this warp's heads) *= alpha; PV of the previous tile
                     // has completed (it was issued before the QK whose commit was just waited for)
@@ -460,40 +481,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_h64_kernel(const __grid_co
                             o[e] = __float_as_uint(__uint_as_float(o[e]) * lds_f32(alpha_s + 4 * (hb + 16 * (c & 1) + e)));
                         tmem_st16(lane_base + col, o);
                     }
-                    tmem_wait_st();
                 }
+                // P and the sums again against the moved references
+                if (ok) (void)score(l_old, l_new, true);
             }
             if (!ok) continue;
-            // ---- P^T row of this key: 2^(z - m) in f16 (0 for a masked key), one 16-byte chunk (8
-            // heads) at a time. P^T of the previous tile was read by its PV, which completed before
-            // this tile's QK did.
-#pragma unroll 1
-            for (int half = 0; half < 2; ++half) {
-                uint32_t sv[16], lv[16];
-                tmem_ld16(lane_base + kColS + hb + 16 * half, sv);
-                tmem_ld16(lane_base + kColL + hb + 16 * half, lv);
-                tmem_wait_ld();
-#pragma unroll
-                for (int c2 = 0; c2 < 2; ++c2) {
-                    uint32_t pw[4];
-#pragma unroll
-                    for (int g2 = 0; g2 < 4; ++g2) {
-                        const int e = 8 * c2 + 2 * g2;     // column in sv / lv
-                        const uint4 c = lds_u128(cm_s + 16 * ((hb >> 1) + 8 * half + (e >> 1)));
-                        const float2 z = f32x2_unpack(f32x2_fma(f32x2_pack(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])),
-                                                                f32x2_pack(__uint_as_float(c.x), __uint_as_float(c.y)),
-                                                                f32x2_pack(__uint_as_float(c.z), __uint_as_float(c.w))));
-                        const float p0 = valid ? ex2_approx(z.x) : 0.0f, p1 = valid ? ex2_approx(z.y) : 0.0f;
-                        const float2 lsum = f32x2_unpack(f32x2_add(f32x2_pack(__uint_as_float(lv[e]), __uint_as_float(lv[e + 1])),
-                                                                   f32x2_pack(p0, p1)));
-                        lv[e] = __float_as_uint(lsum.x);
-                        lv[e + 1] = __float_as_uint(lsum.y);
-                        pw[g2] = pack_f16x2(p0, p1);
-                    }
-                    sts_u128(p_row + (((4 * h2 + 2 * half + c2) ^ (key & 7)) << 4), make_uint4(pw[0], pw[1], pw[2], pw[3]));
-                }
-                tmem_st16(lane_base + kColL + hb + 16 * half, lv);
-            }
             tmem_wait_st();
             fence_proxy_async_smem();
             tc_fence_before_sync();
@@ -515,7 +507,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_h64_kernel(const __grid_co
         float* xl = reinterpret_cast<float*>(smem + kOffK);   // [64 heads][129]
         {
             uint32_t lv[32];
-            tmem_ld32(lane_base + kColL + hb, lv);
+            tmem_ld32(lane_base + kColL + 64 * (n_tiles & 1) + hb, lv);   // the buffer the last tile wrote
             tmem_wait_ld();
 #pragma unroll
             for (int j = 0; j < 32; ++j) xl[(hb + j) * 129 + key] = __uint_as_float(lv[j]);
