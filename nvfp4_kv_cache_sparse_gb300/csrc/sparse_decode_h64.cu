@@ -559,10 +559,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_h64_kernel(const __grid_co
             }
         }
     } else if (warp < kWarpMma) {
-        // ============ converters: K dims 0-511 of keys j and j + 64, 16-dim blocks 4c + q ============
+        // ============ converters: K dims 0-511 of keys j and j + 64, 16-dim blocks 8c + 2q, 8c + 2q + 1 ============
         const int t = threadIdx.x - 32 * kWarpConv;
-        const int q = t & 3;
-        const int j = t >> 2;
+        // lane l of converter warp w: key 8w + (l & 7) (and 64 more), quarter q = l >> 3, so that the
+        // eight lanes of a quarter-warp store to eight different 16-byte bank slots (eight keys, one
+        // q), while the four quarters of a key still load one contiguous 64-byte run per instruction
+        const int q = (t >> 3) & 3;
+        const int j = (t & 7) + 8 * (t >> 5);
         const uint32_t k_s = sbase + kOffK;
         bool ok = !aborted(ctl);
         KeyRaw<R, kBlkOrder> r0, r1;
