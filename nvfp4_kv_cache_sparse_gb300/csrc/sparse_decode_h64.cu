@@ -173,9 +173,8 @@ struct KeyRaw {
     uint4 codes[4];
     uint4 sc[kPermuted ? 1 : 2];
 
-    __device__ __forceinline__ void load(const uint8_t* rec, int q) {
-#pragma unroll
-        for (int c = 0; c < 4; ++c) codes[c] = ldg_stream16(rec + 64 * c + 16 * q);
+    __device__ __forceinline__ void load_codes(const uint8_t* rec, int q, int c) { codes[c] = ldg_stream16(rec + 64 * c + 16 * q); }
+    __device__ __forceinline__ void load_scales(const uint8_t* rec, int q) {
         if constexpr (kPermuted) {
             sc[0] = ldg_stream16(rec + 320 + 16 * (q & 1));
         } else {
@@ -183,6 +182,16 @@ struct KeyRaw {
             sc[0] = ldg_stream16(rec + sb);
             sc[1] = ldg_stream16(rec + sb + 16);
         }
+    }
+    __device__ __forceinline__ void load(const uint8_t* rec, int q) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) load_codes(rec, q, c);
+        load_scales(rec, q);
+    }
+    // the scale pairs of blocks c = 0..3, two per word (c even: low half)
+    __device__ __forceinline__ void scale_pairs(int q, uint32_t (&sp)[2]) const {
+        sp[0] = (scale_pair(0, q) & 0xFFFFu) | (scale_pair(1, q) << 16);
+        sp[1] = (scale_pair(2, q) & 0xFFFFu) | (scale_pair(3, q) << 16);
     }
     // byte 0: the scale of block 8c + 2q, byte 1: of block 8c + 2q + 1
     __device__ __forceinline__ uint32_t scale_pair(int c, int q) const {
@@ -586,6 +595,17 @@ __global__ void __launch_bounds__(kThreads, 1) decode_h64_kernel(const __grid_co
         for (int k = 0; k < n_tiles; ++k) {
             const bool v0 = in_range(i0), v1 = in_range(i1);
             if (q == 0 && ((i0 >= 0 && !v0) || (i1 >= 0 && !v1)) && a.status != nullptr) atomicOr(a.status, 0x2u);
+            // The next tile's record bytes go out as soon as this tile no longer needs the registers
+            // they land in: the scale bytes now (this tile's scale pairs are taken first), the codes of
+            // block b right after block b is converted.
+            uint32_t sp0[2], sp1[2];
+            r0.scale_pairs(q, sp0);
+            r1.scale_pairs(q, sp1);
+            const bool ld0 = in_range(n0), ld1 = in_range(n1);
+            const uint8_t* rec0 = a.cache + static_cast<int64_t>(ld0 ? n0 : 0) * R;
+            const uint8_t* rec1 = a.cache + static_cast<int64_t>(ld1 ? n1 : 0) * R;
+            if (ld0) r0.load_scales(rec0, q);
+            if (ld1) r1.load_scales(rec1, q);
 #pragma unroll
             for (int b = 0; b < 4; ++b) {
                 // dims 128b .. 128b + 127 once the previous tile's PV has read them: 64-dim block
@@ -596,7 +616,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_h64_kernel(const __grid_co
                 const int ch0 = 4 * (q & 1);
                 const uint4 z = make_uint4(0u, 0u, 0u, 0u);
                 {
-                    const uint32_t sp = r0.scale_pair(b, q);
+                    const uint32_t sp = sp0[b >> 1] >> (16 * (b & 1));
                     const __half2 sa = scale_half2(sp & 0xFFu), sb = scale_half2((sp >> 8) & 0xFFu);
                     sts_u128(blk + swz(j, ch0), v0 ? dq8(r0.codes[b].x, sa) : z);
                     sts_u128(blk + swz(j, ch0 + 1), v0 ? dq8(r0.codes[b].y, sa) : z);
@@ -604,7 +624,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_h64_kernel(const __grid_co
                     sts_u128(blk + swz(j, ch0 + 3), v0 ? dq8(r0.codes[b].w, sb) : z);
                 }
                 {
-                    const uint32_t sp = r1.scale_pair(b, q);
+                    const uint32_t sp = sp1[b >> 1] >> (16 * (b & 1));
                     const __half2 sa = scale_half2(sp & 0xFFu), sb = scale_half2((sp >> 8) & 0xFFu);
                     sts_u128(blk + swz(j + 64, ch0), v1 ? dq8(r1.codes[b].x, sa) : z);
                     sts_u128(blk + swz(j + 64, ch0 + 1), v1 ? dq8(r1.codes[b].y, sa) : z);
@@ -614,15 +634,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_h64_kernel(const __grid_co
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&ctl->kfull[b]);
+                if (ld0) r0.load_codes(rec0, q, b);
+                if (ld1) r1.load_codes(rec1, q, b);
             }
             if (!ok) break;
-            // the next tile's record bytes (their indices were loaded a tile ago)
-            i0 = n0;
-            i1 = n1;
-            if (in_range(i0)) r0.load(a.cache + static_cast<int64_t>(i0) * R, q);
-            if (in_range(i1)) r1.load(a.cache + static_cast<int64_t>(i1) * R, q);
             prefetch_record(m0);
             prefetch_record(m1);
+            i0 = n0;
+            i1 = n1;
             n0 = m0;
             n1 = m1;
             m0 = index_at(k + 3, j);
