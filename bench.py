@@ -362,18 +362,37 @@ def run_gpu(args):
     # from pinned host memory and its result out. Device inputs and outputs are double-buffered
     # over three streams (copy in, compute, copy out), so step k+1's upload and step k-1's
     # download overlap step k's kernels, as a caller pipelining these calls would.
-    pin = lambda t: t.pin_memory()
-    host_q = [pin(s.q) for s in sets]
-    host_idx = [pin(s.indices) for s in sets]
-    host_new = [tuple(pin(t) for t in new_token_batch(w0, k)) for k in range(N_SETS)]
-    host_out = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(2)]
-    host_lse = [torch.empty(lse.shape, dtype=lse.dtype).pin_memory() for _ in range(2)]
-    d_q = [torch.empty_like(qs[0]) for _ in range(2)]
-    d_idx = [torch.empty_like(idxs[0]) for _ in range(2)]
-    d_new = [[torch.empty_like(t) for t in news[0]] for _ in range(2)]
-    d_out = [torch.empty_like(out) for _ in range(2)]
-    d_lse = [torch.empty_like(lse) for _ in range(2)]
+    # Each set's inputs (q, indices, the new tokens) sit in one pinned buffer and go up in one copy;
+    # out and lse come back in one copy. The tensors the calls take are views of those buffers.
+    def packed(parts):
+        """Byte offsets of the parts (tensors or (shape, dtype) pairs), each 256-byte aligned."""
+        offs, n = [], 0
+        for shape, dtype in parts:
+            offs.append(n)
+            n += -(-int(np.prod(shape)) * torch.empty((), dtype=dtype).element_size() // 256) * 256
+        return offs, n
+
+    def views(buf, parts, offs):
+        return [buf[o:o + int(np.prod(sh)) * torch.empty((), dtype=dt).element_size()].view(dt).view(sh)
+                for (sh, dt), o in zip(parts, offs)]
+
+    in_parts = [(tuple(t.shape), t.dtype) for t in (sets[0].q, sets[0].indices) + tuple(new_token_batch(w0, 0))]
+    in_offs, in_bytes = packed(in_parts)
+    res_parts = [(tuple(out.shape), out.dtype), (tuple(lse.shape), lse.dtype)]
+    res_offs, res_bytes = packed(res_parts)
+    host_in = []
+    for k in range(N_SETS):
+        buf = torch.empty(in_bytes, dtype=torch.uint8).pin_memory()
+        for v, t in zip(views(buf, in_parts, in_offs), (sets[k].q, sets[k].indices) + tuple(new_token_batch(w0, k))):
+            v.copy_(t)
+        host_in.append(buf)
+    host_res = [torch.empty(res_bytes, dtype=torch.uint8).pin_memory() for _ in range(2)]
+    d_in = [torch.empty(in_bytes, dtype=torch.uint8, device=dev) for _ in range(2)]
+    d_res = [torch.empty(res_bytes, dtype=torch.uint8, device=dev) for _ in range(2)]
+    d_q, d_idx, d_lat, d_rope, d_slots = zip(*[views(d_in[b], in_parts, in_offs) for b in range(2)])
+    d_out, d_lse = zip(*[views(d_res[b], res_parts, res_offs) for b in range(2)])
     s_in, s_comp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    s_default = torch.cuda.current_stream()
     ev_in = [torch.cuda.Event() for _ in range(2)]     # inputs of buffer b uploaded
     ev_used = [torch.cuda.Event() for _ in range(2)]   # kernels done with buffer b
     ev_out = [torch.cuda.Event() for _ in range(2)]    # result of buffer b downloaded
@@ -382,24 +401,21 @@ def run_gpu(args):
 
     def e2e_step(k):
         j, b = k % N_SETS, k % 2
-        with torch.cuda.stream(s_in):
-            s_in.wait_event(ev_used[b])
-            d_q[b].copy_(host_q[j], non_blocking=True)
-            d_idx[b].copy_(host_idx[j], non_blocking=True)
-            for d, h in zip(d_new[b], host_new[j]):
-                d.copy_(h, non_blocking=True)
-            ev_in[b].record(s_in)
+        torch.cuda.set_stream(s_in)
+        s_in.wait_event(ev_used[b])
+        d_in[b].copy_(host_in[j], non_blocking=True)
+        ev_in[b].record(s_in)
         s_comp.wait_event(ev_in[b])
         s_comp.wait_event(ev_out[b])
-        lib.quantize_append(d_new[b][0], d_new[b][1], d_new[b][2], cache, stream=s_comp)
+        lib.quantize_append(d_lat[b], d_rope[b], d_slots[b], cache, stream=s_comp)
         lib.sparse_mla_decode(d_q[b], cache, d_idx[b], w0.sm_scale, out=d_out[b], lse=d_lse[b],
                               num_splits=splits, workspace=workspace, stream=s_comp)
         ev_used[b].record(s_comp)
-        with torch.cuda.stream(s_out):
-            s_out.wait_event(ev_used[b])
-            host_out[b].copy_(d_out[b], non_blocking=True)
-            host_lse[b].copy_(d_lse[b], non_blocking=True)
-            ev_out[b].record(s_out)
+        torch.cuda.set_stream(s_out)
+        s_out.wait_event(ev_used[b])
+        host_res[b].copy_(d_res[b], non_blocking=True)
+        ev_out[b].record(s_out)
+        torch.cuda.set_stream(s_default)
 
     for k in range(args.warmup):
         e2e_step(k)
@@ -414,8 +430,7 @@ def run_gpu(args):
     e2.record(s_in)
     torch.cuda.synchronize()
     t_e2e = max_over_ranks(s2.elapsed_time(e2) / 1e3, world, dev)
-    h2d = sum(t.numel() * t.element_size() for t in (host_q[0], host_idx[0]) + host_new[0])
-    d2h = host_out[0].numel() * host_out[0].element_size() + host_lse[0].numel() * host_lse[0].element_size()
+    h2d, d2h = in_bytes, res_bytes   # bytes copied each step (the parts plus their alignment padding)
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {int(status.item())} after timing")
 

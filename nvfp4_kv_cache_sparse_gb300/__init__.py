@@ -8,6 +8,7 @@ sm_103, the calls raise.
 from __future__ import annotations
 
 import ctypes
+import functools
 import os
 from typing import Optional, Tuple
 
@@ -98,14 +99,15 @@ def status_string(status: int) -> str:
     return load().nvfp4_mla_status_string(int(status)).decode()
 
 
-def _ptr(t: Optional[torch.Tensor]):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+# Pointers and streams go to the C calls as plain integers (their argtypes are c_void_p); None is NULL.
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
 
 
-def _stream(stream) -> ctypes.c_void_p:
+def _stream(stream) -> int:
     if stream is None:
         stream = torch.cuda.current_stream()
-    return ctypes.c_void_p(stream.cuda_stream)
+    return stream.cuda_stream
 
 
 def _check(call: str, status: int):
@@ -138,8 +140,9 @@ def quantize_append(kv_latent: torch.Tensor, k_rope: torch.Tensor, slot_mapping:
     _need(cache.dtype == torch.uint8 and cache.dim() == 2 and cache.is_contiguous(), "cache uint8 [num_slots, R] contiguous")
     _need(cache.shape[1] in RECORD_BYTES, "record width must be 352, 432 or 656")
     code = _record_code(cache, block_scales)
-    for t in (kv_latent, k_rope, slot_mapping, cache):
-        _need(t.is_cuda and t.device == cache.device, "all tensors on the same CUDA device")
+    dev = cache.get_device()   # -1 for a CPU tensor
+    _need(dev >= 0 and all(t.get_device() == dev for t in (kv_latent, k_rope, slot_mapping)),
+          "all tensors on the same CUDA device")
     st = load().nvfp4_mla_quantize_append(
         _ptr(kv_latent), kv_latent.stride(0), _ptr(k_rope), k_rope.stride(0), _ptr(slot_mapping), T,
         _ptr(cache), cache.shape[0], code, _ptr(dev_status), _stream(stream))
@@ -177,6 +180,14 @@ def norm_rope_quantize_append(kv_latent: torch.Tensor, norm_weight: torch.Tensor
         _ptr(positions), _ptr(cos_table), _ptr(sin_table), cos_table.shape[0], int(bool(rotate_half)),
         _ptr(slot_mapping), T, _ptr(cache), cache.shape[0], code, _ptr(dev_status), _stream(stream))
     _check("nvfp4_mla_norm_rope_quantize_append", st)
+
+
+@functools.lru_cache(maxsize=256)
+def _workspace_size_on(device: int, batch: int, s_q: int, h_q: int, topk: int, record_bytes: int,
+                       num_splits: int) -> int:
+    """workspace_size for the given device (the automatic split count depends on its SM count)."""
+    with torch.cuda.device(device):
+        return workspace_size(batch, s_q, h_q, topk, record_bytes, num_splits)
 
 
 def workspace_size(batch: int, s_q: int, h_q: int, topk: int, record_bytes: int, num_splits: int = 0) -> int:
@@ -219,9 +230,10 @@ def sparse_mla_decode(q: torch.Tensor, cache: torch.Tensor, indices: torch.Tenso
         lse = torch.empty((B, s_q, h_q), dtype=torch.float32, device=q.device)
     _need(out.dtype == torch.bfloat16 and out.is_contiguous() and tuple(out.shape) == (B, s_q, h_q, D_V), "out bf16 [B,s_q,h_q,512]")
     _need(lse.dtype == torch.float32 and lse.is_contiguous() and tuple(lse.shape) == (B, s_q, h_q), "lse fp32 [B,s_q,h_q]")
-    for t in (q, cache, indices, out, lse) + ((attn_sink,) if attn_sink is not None else ()):
-        _need(t.is_cuda and t.device == q.device, "all tensors on the same CUDA device")
-    need = workspace_size(B, s_q, h_q, topk, code, num_splits)
+    dev = q.get_device()   # -1 for a CPU tensor
+    _need(dev >= 0 and all(t.get_device() == dev for t in (cache, indices, out, lse)) and
+          (attn_sink is None or attn_sink.get_device() == dev), "all tensors on the same CUDA device")
+    need = _workspace_size_on(dev, B, s_q, h_q, topk, code, num_splits)
     if need and (workspace is None or workspace.numel() * workspace.element_size() < need):
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
