@@ -44,8 +44,10 @@
 //         32 (w >> 2)..+31, and writes the RoPE rows of those keys for the next tile; q staging in
 //         the prologue; row sums, O^T / l and the output in the epilogue
 //   8-15  converters: four threads per key (keys j and j + 64); thread q converts record bytes
-//         64c + 16q .. + 15 (c = 0..3: 16-dim blocks 8c + 2q, 8c + 2q + 1) and holds the next tile's
-//         bytes in registers while the current tile is scored
+//         64c + 16q .. + 15 (c = 0..3: 16-dim blocks 8c + 2q, 8c + 2q + 1). The next tile's bytes
+//         are loaded into registers as soon as this tile no longer needs them (the scale bytes at
+//         the start of a tile, the codes of block c right after block c is converted), and the
+//         records two tiles ahead are prefetched into L2
 //   16    MMA issuer (one elected thread) and tensor-memory owner
 // Every wait is bounded by time; on timeout the CTA sets NVFP4_MLA_DEV_TIMEOUT, stops issuing work,
 // drains what it issued and returns.
@@ -584,7 +586,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_h64_kernel(const __grid_co
         int32_t n0 = index_at(1, j), n1 = index_at(1, j + 64);
         int32_t m0 = index_at(2, j), m1 = index_at(2, j + 64);
         // The records two tiles ahead go into L2 (the four threads of a key touch every 128-byte line
-        // of its record: points 64 apart), so that the register loads a tile ahead find them there.
+        // of its record: points 64 apart), so that the register loads of the next tile find them there.
         auto prefetch_record = [&](int32_t v) {
             if (in_range(v)) {
                 const uint8_t* rec = a.cache + static_cast<int64_t>(v) * R;
