@@ -223,6 +223,15 @@ def roofline_numbers(w: synth.DecodeWorkload):
     return flops, bytes_
 
 
+def roofline_numbers_valid_only(w: synth.DecodeWorkload):
+    """The same counting only the used top-k entries (index >= 0): their records and their share
+    of the contractions (the index list is still read whole)."""
+    used = int((w.indices >= 0).sum())
+    flops = 2.0 * w.h_q * used * (576 + 512)
+    bytes_ = used * w.record_bytes + w.n_rows * (w.h_q * 576 * 2 + w.topk * 4)
+    return flops, bytes_
+
+
 def make_sets(seed: int):
     """N_SETS decode batches over one pool (same pages, different queries and index lists)."""
     sets = [synth.batch_decode(seed=seed + k) for k in range(N_SETS)]
@@ -695,12 +704,15 @@ def measure_decode(w, dev, iters, flush, peaks):
         cold = _time_calls(call, iters, flush)
     flops, bytes_ = roofline_numbers(w)
     t_roof = max(bytes_ / (hbm * 1e9), flops / (tflops * 1e12))
+    vflops, vbytes = roofline_numbers_valid_only(w)
+    t_roof_valid = max(vbytes / (hbm * 1e9), vflops / (tflops * 1e12))
     res = {"kind": "decode", "query_tokens": w.n_rows, "us_per_call_warm": warm * 1e6, "us_per_call_cold": cold * 1e6,
            "query_tokens_per_s_cold": w.n_rows / cold, "roofline_us": t_roof * 1e6, "roofline_frac_cold": t_roof / cold,
            "roofline_frac_warm": t_roof / warm,
            "bound": "tensor" if flops / (tflops * 1e12) > bytes_ / (hbm * 1e9) else "hbm",
            "algorithmic_flops": flops, "algorithmic_bytes": bytes_,
            "valid_index_fraction": int((w.indices >= 0).sum()) / w.indices.numel(), "calls_timed": iters,
+           "roofline_us_valid_only": t_roof_valid * 1e6, "roofline_frac_cold_valid_only": t_roof_valid / cold,
            "clocks": sampler.summary()}
     del cache
     torch.cuda.empty_cache()
