@@ -232,7 +232,7 @@ def _sampled_parity(w: synth.DecodeWorkload, n_rows: int):
 
 
 def test_batch_decode_b32_h128_sampled():
-    _sampled_parity(synth.batch_decode(seed=0), 6)
+    _sampled_parity(synth.batch_decode(seed=0), 8)
 
 
 def test_varlen_mtp_sink_sampled():
@@ -241,11 +241,11 @@ def test_varlen_mtp_sink_sampled():
 
 def test_sparse_prefill_sampled():
     """Sparse prefill / extend: 2 requests x 256 new tokens, causal top-k over a 16K prefix."""
-    _sampled_parity(synth.sparse_prefill(seed=0), 6)
+    _sampled_parity(synth.sparse_prefill(seed=0), 8)
 
 
 def test_long_context_432_sampled():
-    _sampled_parity(synth.long_context(seed=0), 6)
+    _sampled_parity(synth.long_context(seed=0), 8)
 
 
 def test_a_wait_that_runs_out_reports_a_timeout_and_leaves_the_context_usable():
