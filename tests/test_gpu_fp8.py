@@ -96,4 +96,4 @@ def test_small_problems(B, s_q, H, topk, sink, splits):
 def test_batch_decode_b32_h128_656_sampled():
     w = synth.batch_decode(seed=0)
     w = dataclasses.replace(w, name="decode_b32_sq1_h128_topk2048_R656", record_bytes=656)
-    _sampled_parity(w, 6)
+    _sampled_parity(w, 8)
