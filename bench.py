@@ -232,6 +232,23 @@ def roofline_numbers_valid_only(w: synth.DecodeWorkload):
     return flops, bytes_
 
 
+def pack_layout(parts):
+    """Byte offsets of `parts` ((shape, dtype) pairs) laid out one after another in one uint8
+    buffer, each starting on a 256-byte boundary, and the buffer's size."""
+    offs, n = [], 0
+    for shape, dtype in parts:
+        offs.append(n)
+        nbytes = int(np.prod(shape)) * torch.empty((), dtype=dtype).element_size()
+        n += -(-nbytes // 256) * 256
+    return offs, n
+
+
+def pack_views(buf: torch.Tensor, parts, offs):
+    """Typed, shaped views of a uint8 buffer at the offsets pack_layout gave."""
+    return [buf[o:o + int(np.prod(sh)) * torch.empty((), dtype=dt).element_size()].view(dt).view(sh)
+            for (sh, dt), o in zip(parts, offs)]
+
+
 def make_sets(seed: int):
     """N_SETS decode batches over one pool (same pages, different queries and index lists)."""
     sets = [synth.batch_decode(seed=seed + k) for k in range(N_SETS)]
@@ -373,18 +390,7 @@ def run_gpu(args):
     # download overlap step k's kernels, as a caller pipelining these calls would.
     # Each set's inputs (q, indices, the new tokens) sit in one pinned buffer and go up in one copy;
     # out and lse come back in one copy. The tensors the calls take are views of those buffers.
-    def packed(parts):
-        """Byte offsets of the parts (tensors or (shape, dtype) pairs), each 256-byte aligned."""
-        offs, n = [], 0
-        for shape, dtype in parts:
-            offs.append(n)
-            n += -(-int(np.prod(shape)) * torch.empty((), dtype=dtype).element_size() // 256) * 256
-        return offs, n
-
-    def views(buf, parts, offs):
-        return [buf[o:o + int(np.prod(sh)) * torch.empty((), dtype=dt).element_size()].view(dt).view(sh)
-                for (sh, dt), o in zip(parts, offs)]
-
+    packed, views = pack_layout, pack_views
     in_parts = [(tuple(t.shape), t.dtype) for t in (sets[0].q, sets[0].indices) + tuple(new_token_batch(w0, 0))]
     in_offs, in_bytes = packed(in_parts)
     res_parts = [(tuple(out.shape), out.dtype), (tuple(lse.shape), lse.dtype)]
