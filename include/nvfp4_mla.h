@@ -192,10 +192,12 @@ NVFP4_MLA_API int nvfp4_sparse_mla_decode_plan(int32_t batch, int32_t s_q, int32
  *                arguments, 256-byte aligned; may be NULL when that size is 0. Its contents
  *                need no initialization.
  *   dev_status   nullable device uint32 (see NVFP4_MLA_DEV_*).
- * Precision: dequantized NVFP4 keys are exact (bf16 for QK^T, f16 for PV); fp8 keys are
- * e4m3 * scale rounded in fp32 and then to bf16 (QK^T) or f16 (PV); the two contractions
- * run on tcgen05 16-bit MMAs with fp32 accumulation (P enters PV as f16); softmax in fp32;
- * `out` is rounded to bf16 once, after the parts' f16 partial outputs (relative error
+ * Precision: dequantized NVFP4 keys are exact in f16 and enter both contractions as f16, with q
+ * as f16 times a per-head power of two (the same products as bf16 q for every element within
+ * 2^28 of its head's largest |q|; the bf16 RoPE of 432-byte records and its q part stay bf16);
+ * fp8 keys are e4m3 * scale rounded in fp32 and then to bf16 (QK^T) or f16 (PV); the
+ * contractions run on tcgen05 16-bit MMAs with fp32 accumulation (P enters PV as f16); softmax
+ * in fp32; `out` is rounded to bf16 once, after the parts' f16 partial outputs (relative error
  * <= 2^-11 each) are merged in fp32 when the top-k list is split.
  */
 NVFP4_MLA_API int nvfp4_sparse_mla_decode(const void* q, const uint8_t* cache, int64_t num_slots,
