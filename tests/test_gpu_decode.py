@@ -172,6 +172,24 @@ def test_reference_maximum_moves_on_later_tiles(H, R, sm_scale):
         assert_close(out, lse, ref_out, ref_lse)
 
 
+@pytest.mark.parametrize("R", [352, 432])
+def test_more_rows_than_sms_two_parts(R):
+    """64 heads, 200 query rows (between one and two per SM on a 152-SM GB300, so the grid runs in
+    two waves), by the library's choice of parts and with two parts per row; every row is compared
+    with the oracle."""
+    rng = np.random.default_rng(200 + R)
+    B, s_q, H, topk, n_slots = 100, 2, 64, 600, 2000
+    q = rng.standard_normal((B, s_q, H, 576)).astype(np.float32)
+    idx = np.stack([rng.choice(n_slots, size=topk, replace=False) for _ in range(B * s_q)]).reshape(B, s_q, topk)
+    idx = idx.astype(np.int32)
+    idx[rng.random(idx.shape) < 0.1] = -1
+    sink = rng.standard_normal(H).astype(np.float32)
+    for splits in (0, 2):
+        out, lse, ref_out, ref_lse, st = run_small(q, idx, R, n_slots, 41, 1 / math.sqrt(576), sink, splits)
+        assert st == 0
+        assert_close(out, lse, ref_out, ref_lse)
+
+
 def test_many_splits_reused_dirty_workspace_is_deterministic():
     """Five splits with a sink: the partials and their merge depend on nothing left in the
     workspace, so a reused workspace and one filled with junk give the same bits, and those
