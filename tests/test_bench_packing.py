@@ -33,3 +33,17 @@ def test_views_round_trip():
     copy = buf.clone()   # what one byte copy of the buffer carries
     for v, t in zip(bench.pack_views(copy, parts, offs), tensors):
         assert torch.equal(v, t)
+
+
+def test_valid_only_roofline_counts_used_entries():
+    """bench.roofline_numbers_valid_only: only entries >= 0 contribute records and contraction
+    work; q and the whole index lists are always read (the tiny workload masks 8 of 64)."""
+    import synth
+    w = synth.tiny_decode(seed=0)
+    used = int((w.indices >= 0).sum())
+    assert 0 < used < w.indices.numel()
+    flops, bytes_ = bench.roofline_numbers_valid_only(w)
+    assert flops == 2.0 * w.h_q * used * (576 + 512)
+    assert bytes_ == used * w.record_bytes + w.n_rows * (w.h_q * 576 * 2 + w.topk * 4)
+    full_flops, full_bytes = bench.roofline_numbers(w)
+    assert flops < full_flops and bytes_ < full_bytes
